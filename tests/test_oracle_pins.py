@@ -1,0 +1,498 @@
+"""Pins of the float64 oracle to what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: each check is a closed form, a
+special case that reduces to a library routine (numpy, torch CPU float64), a
+brute force on tiny inputs, or a structural fact the pages print
+(tests/golden/tree_examples.json).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import topology as topo_mod
+import workloads as wl
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+def _f32(x):
+    return np.ascontiguousarray(x, np.float32)
+
+
+# ----------------------------------------------------------------------------- heads
+
+def test_heads_zero_w1_equals_lm_head():
+    """W1 = 0 and W2 = the LM head make every head reproduce the base logits.
+
+    Paper review, "Medusa 的三个核心组件": W2 is initialised from the LM head and W1
+    set to zero so the initial predictions equal the backbone's.  With W1 = 0,
+    SiLU(0) = 0, so u = h and z = LM h exactly.
+    """
+    g = np.random.default_rng(7)
+    B, H, V, K, topk = 3, 24, 50, 3, 5
+    h = _f32(g.standard_normal((B, H)))
+    lm = _f32(g.standard_normal((V, H)))
+    w1 = np.zeros((K, H, H), np.float32)
+    w2 = np.stack([lm] * K)
+    r = oracle.heads(h, w1, w2, topk)
+    base = h.astype(np.float64) @ lm.astype(np.float64).T  # library matmul
+    np.testing.assert_allclose(r["u"], np.repeat(h[:, None, :], K, 1), rtol=0, atol=0)
+    for k in range(K):
+        np.testing.assert_allclose(r["z"][:, k], base, rtol=1e-12, atol=1e-12)
+        ref = np.argsort(-base, axis=1, kind="stable")[:, :topk]
+        np.testing.assert_array_equal(r["idx"][:, k], ref)
+
+
+def test_heads_silu_residual_closed_form():
+    """A two-unit head with pre-activations +ln3 and -ln3.
+
+    SiLU(x) = x / (1 + e^-x): SiLU(ln 3) = (3/4) ln 3 and SiLU(-ln 3) = -(1/4) ln 3.
+    h = (1, 2); W1 = [[0, ln3/2], [-ln3, 0]] (rows are outputs) gives
+    a = (ln3, -ln3); with the residual, u = (1 + 0.75 ln3, 2 - 0.25 ln3).
+    W2 = [[1, 0], [0, 1], [1, -1]] gives z = (u0, u1, u0 - u1).
+    The off-diagonal W1 catches a transposed W1; the residual term is visible in u.
+    fp32 rounding of ln 3 bounds the error near 1e-7.
+    """
+    ln3 = math.log(3.0)
+    h = _f32([[1.0, 2.0]])
+    w1 = _f32([[[0.0, ln3 / 2], [-ln3, 0.0]]])
+    w2 = _f32([[[1, 0], [0, 1], [1, -1]]])
+    r = oracle.heads(h, w1, w2, 2)
+    u = np.array([1 + 0.75 * ln3, 2 - 0.25 * ln3])
+    np.testing.assert_allclose(r["u"][0, 0], u, rtol=2e-7)
+    np.testing.assert_allclose(r["z"][0, 0], [u[0], u[1], u[0] - u[1]], rtol=2e-6)
+    assert list(r["idx"][0, 0]) == [0, 1]
+
+
+def test_heads_saturated_silu():
+    """Large positive pre-activations: SiLU(a) = a (to e^-a); large negative: 0.
+
+    With W1 = c * P (P a permutation, c = 60) and h > 0, u = c P h + h up to
+    e^-60; with c = -60, u = h.  z follows by a library matmul.
+    """
+    g = np.random.default_rng(3)
+    H, V = 6, 9
+    h = _f32(1.0 + g.random((1, H)))
+    P = np.eye(H, dtype=np.float32)[[2, 0, 5, 1, 3, 4]]
+    w2 = _f32(g.standard_normal((1, V, H)))
+    for c in (60.0, -60.0):
+        r = oracle.heads(h, _f32(c * P)[None], w2, 3)
+        hd = h[0].astype(np.float64)
+        u = (c * P.astype(np.float64) @ hd if c > 0 else 0) + hd
+        np.testing.assert_allclose(r["u"][0, 0], u, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(r["z"][0, 0], w2[0].astype(np.float64) @ u, rtol=1e-12)
+
+
+def test_heads_bf16_decoding_and_head_indexing():
+    """bf16 inputs are decoded exactly, and head k uses W1[k], W2[k].
+
+    The bf16 run must equal the fp32 run on the decoded values (decoding is
+    exact); each head must equal a one-head run on its own weights.
+    """
+    c = wl.config("tiny", H=32, V=40, K=3)
+    c["dtype"] = "bf16"
+    h = wl.hidden(c)
+    w1, w2 = wl.head_weights(c)
+    rb = oracle.heads(h, w1, w2, 4)
+    rf = oracle.heads(wl.bf16_bits_to_f32(h), wl.bf16_bits_to_f32(w1), wl.bf16_bits_to_f32(w2), 4)
+    np.testing.assert_array_equal(rb["z"], rf["z"])
+    for k in range(3):
+        rk = oracle.heads(h, w1[k:k + 1], w2[k:k + 1], 4)
+        np.testing.assert_array_equal(rb["z"][:, k], rk["z"][:, 0])
+        np.testing.assert_array_equal(rb["idx"][:, k], rk["idx"][:, 0])
+
+
+def test_topk_matches_stable_argsort_with_ties():
+    g = np.random.default_rng(11)
+    x = _f32(np.round(g.standard_normal((6, 300)) * 4) / 4)  # many exact ties
+    idx, val = oracle.topk_f32(x, 17)
+    ref = np.argsort(-x.astype(np.float64), axis=1, kind="stable")[:, :17]
+    np.testing.assert_array_equal(idx, ref)
+    np.testing.assert_array_equal(val, np.take_along_axis(x, ref, 1).astype(np.float64))
+
+
+# ----------------------------------------------------------------------------- topology / tree
+
+def test_tree_examples_from_the_guide(golden_dir):
+    ex = json.load(open(os.path.join(golden_dir, "tree_examples.json")))
+    t = topo_mod.dense(ex["dense_2x2"]["topk_per_head"])
+    assert t.n_nodes == ex["dense_2x2"]["n_nodes"]
+    assert len(t.leaves()) == ex["dense_2x2"]["n_leaves"]
+    assert [int((t.depth == d).sum()) for d in range(3)] == ex["dense_2x2"]["level_sizes"]
+    for key in ("dense_4x2", "dense_4x3"):
+        t = topo_mod.dense(ex[key]["topk_per_head"])
+        assert len(t.leaves()) == ex[key]["n_leaves"]
+    for key in ("choices_standard", "choices_aggressive"):
+        t = topo_mod.from_paths(ex[key]["paths"])
+        assert t.n_nodes == ex[key]["n_nodes"]
+        assert t.max_depth == ex[key]["max_depth"]
+
+
+def test_dense_truncation_counts():
+    """Dense K=4, top-4 capped at 256 nodes: 1 + 4 + 16 + 64 + 171 (root counted)."""
+    t = topo_mod.dense([4, 4, 4, 4], max_nodes=256)
+    assert t.n_nodes == 256
+    assert [int((t.depth == d).sum()) for d in range(5)] == [1, 4, 16, 64, 171]
+
+
+def _check_tree_invariants(t, tokens, pos, mask, root_tok, topk_idx, prefix_len):
+    N = t.n_nodes
+    for n in range(N):
+        row = 0
+        for w in range(mask.shape[1]):
+            row |= int(mask[n, w]) << (32 * w)
+        assert bin(row).count("1") == t.depth[n] + 1
+        if n:
+            p = t.parent[n]
+            assert p < n
+            prow = 0
+            for w in range(mask.shape[1]):
+                prow |= int(mask[p, w]) << (32 * w)
+            assert row == prow | (1 << n)
+    for b in range(tokens.shape[0]):
+        assert tokens[b, 0] == root_tok[b]
+        assert np.all(pos[b] == prefix_len[b] + t.depth)
+        for n in range(1, N):
+            assert tokens[b, n] == topk_idx[b][t.depth[n] - 1][t.rank[n]]
+
+
+@pytest.mark.parametrize("kind", ["chain", "dense", "choices", "greedy"])
+def test_tree_build_invariants(kind):
+    g = np.random.default_rng(5)
+    if kind == "chain":
+        t = topo_mod.dense([1] * 5)
+    elif kind == "dense":
+        t = topo_mod.dense([3, 2, 2])
+    elif kind == "choices":
+        t = topo_mod.from_paths([[0], [1], [0, 0], [0, 1], [1, 0], [0, 0, 0], [0, 1, 2]])
+    else:
+        t = topo_mod.greedy(topo_mod.synthetic_accuracy(4, 10), 64)
+    K = max(1, t.max_depth)
+    B = 3
+    topk_idx = g.integers(0, 1000, (B, K, 10)).astype(np.int32)
+    root = g.integers(0, 1000, B).astype(np.int32)
+    pl = np.array([0, 17, 1000], np.int32)
+    tokens, pos, mask = topo_mod.tree_build(t, root, topk_idx, pl)
+    _check_tree_invariants(t, tokens, pos, mask, root, topk_idx, pl)
+    if kind == "chain":
+        dense_mask = np.array([[(mask[i, j // 32] >> (j % 32)) & 1 for j in range(t.n_nodes)]
+                               for i in range(t.n_nodes)])
+        np.testing.assert_array_equal(dense_mask, np.tril(np.ones((t.n_nodes, t.n_nodes), int)))
+
+
+def _closed_sets(children_of, size):
+    """All ancestor-closed node sets of the given size that contain the root."""
+    seen = set()
+    frontier = [frozenset([()])]
+    for _ in range(size - 1):
+        nxt = set()
+        for s in frontier:
+            for p in s:
+                for c in children_of(p):
+                    if c not in s:
+                        nxt.add(s | {c})
+        frontier = list(nxt)
+    seen.update(frontier)
+    return seen
+
+
+def test_greedy_is_optimal_on_a_tiny_table():
+    """For every budget, the greedy tree maximises the summed reach probability.
+
+    Brute force over all ancestor-closed sets of that size (3 heads x 3 ranks).
+    """
+    acc = [[0.7, 0.2, 0.05], [0.5, 0.3, 0.1], [0.45, 0.25, 0.2]]
+
+    def children_of(p):
+        return [p + (r,) for r in range(3)] if len(p) < 3 else []
+
+    for n in range(2, 8):
+        t = topo_mod.greedy(acc, n)
+        got = sum(topo_mod.path_score(acc, p) for p in t.paths[1:])
+        best = max(sum(topo_mod.path_score(acc, p) for p in s if p) for s in _closed_sets(children_of, n))
+        assert got == pytest.approx(best, rel=1e-12)
+
+
+def test_greedy_64_node_tree_is_the_top_63_paths():
+    """With the synthetic table acc[k][i] = 0.6 * 0.8^k * 0.7^i every child scores
+    below its parent, so the best ancestor-closed 64-node set is the root plus the
+    63 highest-scoring paths (depth <= 4, rank < 10).  Checked by sorting all
+    11110 candidate paths."""
+    acc = topo_mod.synthetic_accuracy(4, 10)
+    t = topo_mod.greedy(acc, 64)
+    allp = [p for d in range(1, 5) for p in itertools.product(range(10), repeat=d)]
+    scores = sorted((topo_mod.path_score(acc, p) for p in allp), reverse=True)
+    got = sorted((topo_mod.path_score(acc, p) for p in t.paths[1:]), reverse=True)
+    np.testing.assert_allclose(got, scores[:63], rtol=1e-12)
+    assert t.n_nodes == 64 and t.paths[0] == ()
+    assert all(len(p) <= 4 and max(p) < 10 for p in t.paths[1:])
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _sdpa(q, k, v, scale, mask=None):
+    """torch CPU float64 scaled-dot-product attention (library routine)."""
+    qt, kt, vt = (torch.from_numpy(np.asarray(x, np.float64)) for x in (q, k, v))
+    m = None if mask is None else torch.from_numpy(mask)
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, scale=scale).numpy()
+
+
+def _attn_inputs(c, t, prefix_len, seed_cfg=None):
+    N = t.n_nodes
+    q = wl.queries(c, N)
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    _, _, mask = topo_mod.tree_build(t, np.zeros(c["B"], np.int32), np.zeros((c["B"], max(1, t.max_depth), 10), np.int32),
+                                     prefix_len)
+    return q, kc, vc, kt, vt, mask
+
+
+def test_chain_tree_equals_causal_attention():
+    """Paper FAQ (tree attention): a chain-shaped tree is ordinary causal attention."""
+    c = wl.config("tiny", nl=2, B=2, Hq=2, Hkv=2, d=16, L=9)
+    t = topo_mod.dense([1] * 5)
+    pl = np.array([9, 4], np.int32)
+    q, kc, vc, kt, vt, mask = _attn_inputs(c, t, pl)
+    out = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    N = t.n_nodes
+    for l in range(2):
+        for b in range(2):
+            L = pl[b]
+            keys = np.concatenate([kc[l, b, :L], kt[l, b]], 0)  # [L+N, H, d]
+            vals = np.concatenate([vc[l, b, :L], vt[l, b]], 0)
+            causal = np.tril(np.ones((N, L + N), bool), k=L)
+            ref = _sdpa(q[l, b].transpose(1, 0, 2), keys.transpose(1, 0, 2), vals.transpose(1, 0, 2),
+                        1 / math.sqrt(c["d"]), causal)
+            np.testing.assert_allclose(out[l, b], ref.transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_each_node_equals_attention_on_prefix_plus_ancestor_path(G):
+    """Brute force: every node of a branching tree, one at a time, against
+    attention over the explicit key list prefix + ancestors + itself (paper,
+    "只允许 token 回看自身分支前驱的注意力掩码")."""
+    c = wl.config("tiny", nl=1, B=2, Hq=2 * G, Hkv=2, d=8, L=6)
+    t = topo_mod.from_paths([[0], [1], [2], [0, 0], [0, 1], [1, 0], [0, 0, 0], [0, 1, 0], [1, 0, 1],
+                             [0, 0, 0, 0], [0, 0, 0, 1], [2, 0], [2, 1], [2, 1, 0]])
+    pl = np.array([6, 0], np.int32)
+    q, kc, vc, kt, vt, mask = _attn_inputs(c, t, pl)
+    out = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    for b in range(2):
+        L = pl[b]
+        for i in range(t.n_nodes):
+            anc = []
+            a = i
+            while a >= 0:
+                anc.append(a)
+                a = t.parent[a]
+            anc = anc[::-1]
+            for hq in range(c["Hq"]):
+                g = hq // G
+                keys = np.concatenate([kc[0, b, :L, g], kt[0, b, anc, g]], 0)
+                vals = np.concatenate([vc[0, b, :L, g], vt[0, b, anc, g]], 0)
+                ref = _sdpa(q[0, b, i, hq][None], keys, vals, 1 / math.sqrt(c["d"]))[0]
+                np.testing.assert_allclose(out[0, b, i, hq], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_single_node_is_plain_decode_attention_and_gqa_grouping():
+    """N = 1 is decode attention; q head h reads kv head h // G (torch enable_gqa)."""
+    c = wl.config("tiny", nl=1, B=1, Hq=8, Hkv=2, d=16, L=33)
+    t = topo_mod.from_paths([])
+    pl = np.array([33], np.int32)
+    q, kc, vc, kt, vt, mask = _attn_inputs(c, t, pl)
+    out = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    keys = np.concatenate([kc[0, 0, :33], kt[0, 0]], 0).transpose(1, 0, 2)
+    vals = np.concatenate([vc[0, 0, :33], vt[0, 0]], 0).transpose(1, 0, 2)
+    qt, kt_, vt_ = (torch.from_numpy(np.asarray(x, np.float64)) for x in (q[0, 0].transpose(1, 0, 2), keys, vals))
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt_, vt_, scale=1 / 4.0, enable_gqa=True).numpy()
+    np.testing.assert_allclose(out[0, 0], ref.transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_ignores_cache_rows_past_the_prefix_and_zero_q_averages():
+    """Rows at and past prefix_len never contribute (NaN planted there), and with
+    q = 0 every visible key scores equally, so the output is the mean of the
+    visible value rows (closed form)."""
+    c = wl.config("tiny", nl=1, B=2, Hq=2, Hkv=1, d=8, L=5)
+    t = topo_mod.dense([2, 2])
+    pl = np.array([5, 2], np.int32)
+    q, kc, vc, kt, vt, mask = _attn_inputs(c, t, pl)
+    kc = kc.copy(); vc = vc.copy()
+    for b in range(2):
+        kc[:, b, pl[b]:] = np.nan
+        vc[:, b, pl[b]:] = np.nan
+    out = oracle.tree_attention(np.zeros_like(q), kc, vc, kt, vt, mask, pl)
+    assert np.all(np.isfinite(out))
+    for b in range(2):
+        for i in range(t.n_nodes):
+            anc = []
+            a = i
+            while a >= 0:
+                anc.append(a)
+                a = t.parent[a]
+            rows = np.concatenate([vc[0, b, :pl[b], 0], vt[0, b, anc, 0]], 0).astype(np.float64)
+            for hq in range(2):
+                np.testing.assert_allclose(out[0, b, i, hq], rows.mean(0), rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- typical acceptance
+
+def _golden_tree():
+    # root 0 -> n1 (token 3), n2 (token 1); n1 -> n3 (token 0); n2 -> n4 (token 2)
+    parent = np.array([-1, 0, 0, 1, 2], np.int32)
+    tokens = np.array([[7, 3, 1, 0, 2]], np.int32)
+    return parent, tokens
+
+
+def test_typical_acceptance_worked_example():
+    """Every node carries p = (1/2, 1/4, 1/8, 1/8) (logits = ln p, T = 1).
+
+    Entropy H = (1/2 + 2/4 + 2*3/8) ln 2 = 1.75 ln 2, so exp(-H) = 2^-1.75.
+    With eps = 0.2, delta = 0.5: threshold = min(0.2, 0.5 * 2^-1.75) = 0.148651.
+    n1 (p 1/8) fails, n2 (p 1/4) passes, n4 (p 1/8) fails, and n3 (p 1/2) passes its
+    own test but its parent failed (longest valid prefix).  So the accepted set is
+    {0, 2}, accept_len = 2, path = (0, 2, -1), next token = argmax at n2 = 0.
+    """
+    parent, tokens = _golden_tree()
+    lg = np.log(np.array([0.5, 0.25, 0.125, 0.125]))
+    logits = _f32(np.tile(lg, (1, 5, 1)))
+    r = oracle.typical_accept(logits, tokens, parent, T=1.0, eps=0.2, delta=0.5)
+    thr = 0.5 * 2 ** -1.75
+    assert r["accept_len"][0] == 2
+    assert list(r["path_nodes"][0]) == [0, 2, -1]
+    assert r["next_tok"][0] == 0
+    np.testing.assert_allclose(r["p_tok"][0], [1, 0.125, 0.25, 0.5, 0.125], rtol=1e-6)
+    np.testing.assert_allclose(r["thr"][0, 1:], thr, rtol=1e-6)
+    assert list(r["accepted"][0]) == [True, False, True, False, False]
+    # eps below the entropy term: threshold = eps = 0.1 -> n1 and n4 now pass too
+    r = oracle.typical_accept(logits, tokens, parent, T=1.0, eps=0.1, delta=0.5)
+    np.testing.assert_allclose(r["thr"][0, 1:], 0.1, rtol=1e-12)
+    assert list(r["accepted"][0]) == [True, True, True, True, True]
+    assert r["accept_len"][0] == 3 and list(r["path_nodes"][0]) == [0, 1, 3]
+
+
+def test_typical_acceptance_uniform_closed_form():
+    """Uniform logits: p = 1/V and H = ln V, so the threshold is min(eps, delta / V).
+    delta = 0.5 accepts every node (1/V > 0.5/V); delta = 2 (eps = 1) rejects all."""
+    V = 64
+    t = topo_mod.dense([2, 2, 2])
+    B = 2
+    tokens = np.random.default_rng(1).integers(0, V, (B, t.n_nodes)).astype(np.int32)
+    logits = np.zeros((B, t.n_nodes, V), np.float32)
+    r = oracle.typical_accept(logits, tokens, t.parent, T=0.8, eps=1.0, delta=0.5)
+    np.testing.assert_allclose(r["thr"][:, 1:], 0.5 / V, rtol=1e-12)
+    np.testing.assert_allclose(r["p_tok"][:, 1:], 1.0 / V, rtol=1e-12)
+    assert np.all(r["accept_len"] == 4)
+    assert np.all(r["path_nodes"] == [0, 1, 3, 7])  # first deepest node in canonical order
+    assert np.all(r["next_tok"] == 0)  # argmax of a constant row = lowest index
+    r = oracle.typical_accept(logits, tokens, t.parent, T=0.8, eps=1.0, delta=2.0)
+    assert np.all(r["accept_len"] == 1) and np.all(r["path_nodes"][:, 1:] == -1)
+
+
+def test_temperature_zero_is_argmax_match():
+    """Paper review, "方法细节": at temperature 0 the typical test is greedy decoding.
+
+    Checked against numpy argmax: a node is accepted iff its token equals the
+    argmax of its parent's logits and its parent is accepted.
+    """
+    c = wl.config("tiny", V=50, B=4)
+    t = topo_mod.dense([3, 3])
+    N = t.n_nodes
+    tokens = wl.random_tokens(c, N)
+    logits = wl.plant(c, wl.base_logits(c, N), tokens, t.parent, prob=0.7)
+    r = oracle.typical_accept(logits, tokens, t.parent, T=0.0, eps=0.09, delta=0.3)
+    am = logits.argmax(-1)
+    for b in range(4):
+        ok = [True] + [False] * (N - 1)
+        for n in range(1, N):
+            ok[n] = ok[t.parent[n]] and tokens[b, n] == am[b, t.parent[n]]
+        assert list(r["accepted"][b]) == ok
+        assert r["next_tok"][b] == am[b, r["path_nodes"][b, r["accept_len"][b] - 1]]
+
+
+def test_root_always_accepted_prefix_and_and_longest_path():
+    """First token accepted unconditionally; no accepted node under a rejected one;
+    accept_len = depth of the deepest accepted node + 1; path is root..best."""
+    c = wl.config("tiny", V=300, B=6)
+    t = topo_mod.greedy(topo_mod.synthetic_accuracy(4, 4), 30)
+    N = t.n_nodes
+    tokens = wl.random_tokens(c, N)
+    logits = wl.plant(c, wl.base_logits(c, N), tokens, t.parent, prob=0.8)
+    for T in (0.0, 0.5, 1.0):
+        r = oracle.typical_accept(logits, tokens, t.parent, T=T, eps=0.09, delta=0.3)
+        for b in range(6):
+            acc = r["accepted"][b]
+            assert acc[0]
+            for n in range(1, N):
+                assert not (acc[n] and not acc[t.parent[n]])
+            deepest = max(t.depth[n] for n in range(N) if acc[n])
+            assert r["accept_len"][b] == deepest + 1
+            path = r["path_nodes"][b]
+            best = path[deepest]
+            assert acc[best] and t.depth[best] == deepest
+            assert best == min(n for n in range(N) if acc[n] and t.depth[n] == deepest)
+            for dd in range(deepest + 1):
+                assert t.depth[path[dd]] == dd
+                if dd:
+                    assert t.parent[path[dd]] == path[dd - 1]
+
+
+def test_eps_zero_accepts_every_node():
+    c = wl.config("tiny", V=200, B=3)
+    t = topo_mod.dense([2, 3, 2])
+    tokens = wl.random_tokens(c, t.n_nodes)
+    r = oracle.typical_accept(wl.base_logits(c, t.n_nodes), tokens, t.parent, T=0.7, eps=0.0, delta=0.3)
+    assert np.all(r["accept_len"] == 4)
+    assert np.all(r["accepted"])
+
+
+def test_higher_temperature_accepts_longer_on_average():
+    """Paper review, "方法细节": higher temperature gives longer accepts."""
+    c = wl.config("tiny", V=2000, B=24)
+    t = topo_mod.greedy(topo_mod.synthetic_accuracy(4, 4), 40)
+    tokens = wl.random_tokens(c, t.n_nodes)
+    logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=0.5, margin=1.0)
+    means = [oracle.typical_accept(logits, tokens, t.parent, T=T, eps=0.09, delta=0.3)["accept_len"].mean()
+             for T in (0.0, 1.0, 3.0)]
+    assert means[0] <= means[1] <= means[2] and means[0] < means[2]
+
+
+# ----------------------------------------------------------------------------- kv compaction
+
+def test_kv_compact_chain_full_accept_is_identity_and_other_rows_untouched():
+    c = wl.config("tiny", nl=2, B=2, Hkv=2, d=8, L=10, dtype="bf16")
+    t = topo_mod.dense([1] * 4)
+    N = t.n_nodes
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    pl = np.array([10, 3], np.int32)
+    path = np.tile(np.arange(N, dtype=np.int32), (2, 1))
+    acc = np.array([N, N], np.int32)
+    kc2, vc2, new_len, ovf = oracle.kv_compact(kc, vc, kt, vt, path, acc, pl)
+    assert not ovf.any() and list(new_len) == [10 + N, 3 + N]
+    for b in range(2):
+        L = pl[b]
+        np.testing.assert_array_equal(kc2[:, b, L:L + N], kt[:, b])
+        np.testing.assert_array_equal(vc2[:, b, L:L + N], vt[:, b])
+        np.testing.assert_array_equal(kc2[:, b, :L], kc[:, b, :L])
+        np.testing.assert_array_equal(kc2[:, b, L + N:], kc[:, b, L + N:])
+
+
+def test_kv_compact_overflow_writes_nothing():
+    c = wl.config("tiny", nl=1, B=2, Hkv=1, d=4, L=4)
+    kc, vc = wl.kv_cache(c)  # Lmax = L + slack
+    kt, vt = wl.tree_kv(c, 3)
+    Lmax = kc.shape[2]
+    pl = np.array([Lmax - 1, 0], np.int32)
+    path = np.array([[0, 1, 2], [0, 2, -1]], np.int32)
+    acc = np.array([3, 2], np.int32)
+    kc2, vc2, new_len, ovf = oracle.kv_compact(kc, vc, kt, vt, path, acc, pl)
+    assert list(ovf) == [True, False]
+    np.testing.assert_array_equal(kc2[:, 0], kc[:, 0])
+    assert list(new_len) == [Lmax - 1, 2]
+    np.testing.assert_array_equal(kc2[0, 1, 1], kt[0, 1, 2])
