@@ -1,0 +1,428 @@
+"""Benchmark of one Medusa verify step (heads, tree packing, tree attention over
+all layers, typical acceptance, KV compaction) on GB300.
+
+Workload (default): the Vicuna-7B shape, bf16, batch 1, prefix 1024, 64-node
+greedy sparse tree, T = 0.7, eps = 0.09, delta = 0.3; synthetic seeded inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is verify steps/s of the whole job (N replicas,
+one per GPU: the step does not shard, so N > 1 runs independent replicas).
+The timed region holds exactly K steps, bracketed by a barrier and a device
+synchronisation; per-step inputs (1.18 GB of head weights, 0.57 GB of KV cache)
+are larger than L2, so no flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "Medusa verify steps/s, accepted tok/s; tree-attn & head HBM GB/s vs peak (7B, 64 nodes)"
+UNIT = "verify steps/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def workload_name(c):
+    return (f"vicuna-7b-shape verify step: B={c['B']} H={c['H']} V={c['V']} K={c['K']} top-{c['topk']}, "
+            f"{c['nl']} layers x {c['Hq']} heads x d{c['d']}, prefix {c['L']}, "
+            f"{c['tree'][2]}-node greedy sparse tree, T={c['T']} eps={c['eps']} delta={c['delta']}")
+
+
+def config_json(c, n_nodes):
+    return {"workload": workload_name(c), "batch": c["B"], "hidden": c["H"], "vocab": c["V"], "heads": c["K"],
+            "topk": c["topk"], "layers": c["nl"], "q_heads": c["Hq"], "kv_heads": c["Hkv"], "head_dim": c["d"],
+            "prefix": c["L"], "tree_nodes": n_nodes, "temperature": c["T"], "eps": c["eps"], "delta": c["delta"],
+            "l2": "inputs larger than L2 (1.18 GB head weights + 0.57 GB KV cache read per step), no flush",
+            "parallelism": "replicas (one independent verify step per GPU)"}
+
+
+def algorithmic_bytes(c, N):
+    """Bytes each call must move at least once (reads + writes)."""
+    B, H, V, K, topk = c["B"], c["H"], c["V"], c["K"], c["topk"]
+    es = 2 if c["dtype"] == "bf16" else 4
+    heads = K * (H * H + V * H) * es + B * H * es + B * K * topk * 8
+    nl, Hq, Hkv, d, L = c["nl"], c["Hq"], c["Hkv"], c["d"], c["L"]
+    attn = nl * B * (2 * L * Hkv * d + 2 * N * Hkv * d + 2 * N * Hq * d) * es + N * ((N + 31) // 32) * 4
+    accept = B * N * V * 4 + B * N * 4
+    return {"heads": heads, "attention": attn, "accept": accept}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (200 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def make_inputs(c, N, layers=None):
+    inp = wl.step_inputs(c, N, layers=layers)
+    return inp
+
+
+def run_ours(args, c):
+    import torch
+    import torch.distributed as dist
+    import medusa_head_speculative_heads_gb300 as mg
+    from medusa_head_speculative_heads_gb300.build import build as build_lib
+    from medusa_head_speculative_heads_gb300.step import VerifyStep
+    from oracle import topology as otopo
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build_lib()
+    if world > 1:
+        dist.barrier()
+    mg.lib()
+
+    topo = mg.Topology.greedy(np.array(otopo.synthetic_accuracy(c["K"], c["tree"][1])), c["tree"][2])
+    N = topo.n_nodes
+    inp = make_inputs(c, N)
+    tdev = lambda a: _to_dev(a, dev)  # noqa: E731
+    d = {k: tdev(inp[k]) for k in ("h", "w1", "w2", "root_tok", "prefix_len", "q", "kc", "vc", "kt", "vt",
+                                   "logits")}
+    vs = VerifyStep(B=c["B"], H=c["H"], V=c["V"], K=c["K"], topk=c["topk"], nl=c["nl"], Hq=c["Hq"], Hkv=c["Hkv"],
+                    d=c["d"], Lmax=c["Lmax"], dtype=torch.bfloat16, topology=topo, temperature=c["T"],
+                    eps=c["eps"], delta=c["delta"], device=dev)
+    # Plant the synthetic backbone's agreement on this step's own tree tokens
+    # (untimed set-up: the logits are an input of the step).
+    vs.heads(d["h"], d["w1"], d["w2"])
+    vs.tree(d["root_tok"], d["prefix_len"])
+    torch.cuda.synchronize()
+    tokens = vs.tokens.cpu().numpy()
+    inp["logits"] = wl.plant(c, inp["logits"], tokens, topo.parent)
+    d["logits"] = tdev(inp["logits"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vs.run(d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"],
+               d["vt"], d["logits"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if vs.check() != 0:
+        raise RuntimeError("device status set during warm-up")
+    if args.profile:
+        # Only the named call, `steps` times (for profiler captures; prints no bench line).
+        call = {"heads": lambda: vs.heads(d["h"], d["w1"], d["w2"], stream),
+                "attention": lambda: vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"],
+                                                  stream),
+                "accept": lambda: vs.accept(d["logits"], stream)}[args.profile]
+        for _ in range(args.steps):
+            call()
+        torch.cuda.synchronize()
+        print(f"profile {args.profile}: {args.steps} calls done")
+        return
+
+    # ---- timed region (device events; per-call events on the launching stream)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        vs.heads(d["h"], d["w1"], d["w2"], stream)
+        e[1].record(stream)
+        vs.tree(d["root_tok"], d["prefix_len"], stream)
+        e[2].record(stream)
+        vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"], stream)
+        e[3].record(stream)
+        vs.accept(d["logits"], stream)
+        e[4].record(stream)
+        vs.compact(d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"], stream)
+        e[5].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    names = ["heads", "tree_build", "attention", "accept", "compact"]
+    per_call = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j, n in enumerate(names)}
+    accept_len = vs.accept_len.float().mean().item()
+    assert vs.check() == 0
+
+    ms_per_step = elapsed_ms / K
+    value = world / (ms_per_step / 1e3)
+    hbm, tflops, peak_src = _peaks()
+    ab = algorithmic_bytes(c, N)
+    rooflines = {}
+    for n in ("heads", "attention", "accept"):
+        gbs = ab[n] / (per_call[n] * 1e-3) / 1e9
+        rooflines[n] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(gbs / hbm, 4), "algorithmic_bytes": ab[n], "us": round(per_call[n] * 1e3, 2)}
+    dominant = max(("heads", "attention"), key=lambda n: per_call[n])
+    roof = dict(rooflines[dominant])
+    roof["kernel"] = {"heads": "medusa_heads", "attention": "medusa_tree_attention"}[dominant]
+    roof["peak_source"] = f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback 6.8 TB/s"
+    roof["traffic"] = _traffic(roof["kernel"])
+
+    e2e = run_e2e(args, c, vs, inp, d, dev, stream) if rank == 0 or world > 1 else None
+    cpu = cpu_baseline(c, inp, topo) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, model shapes)",
+                "config": config_json(c, N),
+                "accepted_tok_per_s": round(value * c["B"] * accept_len, 2), "mean_accept_len": accept_len,
+                "per_call_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
+                "roofline": roof, "rooflines": rooflines, "e2e": e2e, "cpu_baseline": cpu,
+                "gpu_launches": K * vs.launches_per_step(), "clocks": clocks}
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        ent = t.get(kernel)
+        if not ent:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, "medusa_head_speculative_heads_gb300", "csrc", ent["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["source_sha"]:
+            return None
+        return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def _to_dev(a, dev):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def run_e2e(args, c, vs, inp, d, dev, stream):
+    """Same step through the public calls with host buffers: every step copies
+    its per-step inputs (hidden state, root token, prefix length, the verify
+    pass's q and tree k/v, the base logits at the tree nodes) from pinned host
+    memory and reads back the step's results (accept length, path, next token,
+    new cache length).  Weights and the KV cache stay resident (model state)."""
+    import torch
+    names = ["h", "root_tok", "prefix_len", "q", "kt", "vt", "logits"]
+    host = {}
+    for k in names:
+        t = _to_dev(inp[k], "cpu")
+        host[k] = t.pin_memory()
+    outs = [vs.accept_len, vs.path_nodes, vs.next_tok, vs.new_len]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step():
+        for k in names:
+            d[k].copy_(host[k], non_blocking=True)
+        vs.run(d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"],
+               d["vt"], d["logits"], stream=stream)
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": round(world / (ms / 1e3), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def oracle_sample(c, inp, topo_o, small=False):
+    """Times the float64 oracle on a bounded sample of one verify step and
+    extrapolates to the whole step by multiply-add counts.
+
+    Full sample: heads (all K heads), tree attention on layer 0 (x nl),
+    acceptance and packing in full, compaction on layer 0 (x nl).
+    Small sample: head 0 with the first V/8 vocabulary rows (scaled by MACs),
+    attention on layer 0 and the first 4 kv heads (x nl*Hkv/4), the rest as
+    above."""
+    import oracle
+    from oracle import topology as otopo
+    K, H, V = c["K"], c["H"], c["V"]
+    t0 = time.perf_counter()
+    if small:
+        vs = max(c["topk"], V // 8)
+        heads = oracle.heads(inp["h"], inp["w1"][:1], inp["w2"][:1, :vs], c["topk"])
+        heads_scale = K * (H * H + V * H) / (H * H + vs * H)
+        idx = np.repeat(heads["idx"], K, axis=1)
+    else:
+        heads = oracle.heads(inp["h"], inp["w1"], inp["w2"], c["topk"])
+        heads_scale = 1.0
+        idx = heads["idx"]
+    t1 = time.perf_counter()
+    tokens, pos, mask = otopo.tree_build(topo_o, inp["root_tok"], idx, inp["prefix_len"])
+    t2 = time.perf_counter()
+    G = c["Hq"] // c["Hkv"]
+    nkv = 4 if small else c["Hkv"]
+    q = np.ascontiguousarray(inp["q"][:1, :, :, :nkv * G])
+    kc, vc = np.ascontiguousarray(inp["kc"][:1, :, :, :nkv]), np.ascontiguousarray(inp["vc"][:1, :, :, :nkv])
+    kt, vt = np.ascontiguousarray(inp["kt"][:1, :, :, :nkv]), np.ascontiguousarray(inp["vt"][:1, :, :, :nkv])
+    t2b = time.perf_counter()
+    oracle.tree_attention(q, kc, vc, kt, vt, mask, inp["prefix_len"])
+    t3 = time.perf_counter()
+    attn_scale = c["nl"] * c["Hkv"] / nkv
+    acc = oracle.typical_accept(inp["logits"], tokens, topo_o.parent, c["T"], c["eps"], c["delta"],
+                                Dmax=topo_o.max_depth)
+    t4 = time.perf_counter()
+    oracle.kv_compact(inp["kc"][:1], inp["vc"][:1], inp["kt"][:1], inp["vt"][:1], acc["path_nodes"],
+                      acc["accept_len"], inp["prefix_len"])
+    t5 = time.perf_counter()
+    step_s = (t1 - t0) * heads_scale + (t2 - t1) + (t3 - t2b) * attn_scale + (t4 - t3) + (t5 - t4) * c["nl"]
+    work = (t1 - t0) + (t2 - t1) + (t3 - t2b) + (t4 - t3) + (t5 - t4)
+    if small:
+        what = (f"head 0 on the first {V // 8} of {V} vocabulary rows (x{heads_scale:.1f} by MACs), "
+                f"tree attention on layer 0 x {nkv} of {c['Hkv']} kv heads (x{attn_scale:g})")
+    else:
+        what = f"heads in full, tree attention on layer 0 of {c['nl']} (x{attn_scale:g})"
+    sample = (f"{what}; tree packing and typical acceptance in full; KV compaction on layer 0 (x{c['nl']}); "
+              f"{work:.2f} s of CPU work per sample, single thread")
+    return step_s, sample, work
+
+
+def cpu_baseline(c, inp, topo):
+    from oracle import topology as otopo
+    topo_o = otopo.greedy(otopo.synthetic_accuracy(c["K"], c["tree"][1]), c["tree"][2])
+    step_s, sample, _ = oracle_sample(c, inp, topo_o)
+    return {"value": round(1.0 / step_s, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args, c):
+    """The oracle as it stands, timed on the host cores (single thread)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import topology as otopo
+    import oracle
+    oracle.build()
+    topo_o = otopo.greedy(otopo.synthetic_accuracy(c["K"], c["tree"][1]), c["tree"][2])
+    # Only layer 0 of the per-layer tensors is generated: the sample times one
+    # layer of attention and scales it (the oracle's cost does not depend on
+    # the values, so the logits are left unplanted here).
+    inp = make_inputs(c, topo_o.n_nodes, layers=[0])
+    for _ in range(args.warmup):
+        oracle_sample(c, inp, topo_o, small=True)
+    times, sample = [], ""
+    for _ in range(args.steps):
+        s, sample, _ = oracle_sample(c, inp, topo_o, small=True)
+        times.append(s)
+    ms = 1e3 * sum(times) / len(times)
+    value = 1e3 / ms
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+                      "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic (seeded, model shapes)", "config": config_json(c, topo_o.n_nodes),
+                      "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                       "sample": sample, "host_cpus": os.cpu_count()},
+                      "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--profile", choices=["heads", "attention", "accept"], default=None,
+                    help="run only this call `steps` times after warm-up (profiler captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    c = wl.config("7b")
+    if args.impl == "reference":
+        run_reference(args, c)
+    else:
+        run_ours(args, c)
+
+
+if __name__ == "__main__":
+    main()

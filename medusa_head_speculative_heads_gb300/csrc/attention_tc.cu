@@ -1,0 +1,531 @@
+// Tree attention on tcgen05 tensor cores: bf16 q/k/v, head_dim 128, fp32
+// scores/accumulators in tensor memory.
+//
+// Paper review ("Medusa: Simple LLM Inference Acceleration Framework with
+// Multiple Decoding Heads"), section "Medusa 的三个核心组件" and FAQ
+// "树注意力为什么能一次验证多条候选": every tree node attends to the shared prefix
+// and to its own ancestors only, all candidates in one pass.
+//
+// Work item: (layer x row, head group, row tile).  The 128 MMA rows of a tile
+// are query rows (node, q head of the GQA group).  When one kv head has at most
+// 64 query rows (the 64-node trees with G = 1), two kv heads share a tile:
+// rows 0-63 belong to head A and 64-127 to head B, the key tile holds 64 keys
+// of A (columns 0-63) and the same 64 key positions of B (columns 64-127), and
+// the off-diagonal score blocks are masked, so P is block-diagonal and PV
+// keeps the heads apart.  This keeps all four TMEM lane quarters (and the four
+// SM sub-partitions' exp units) busy.  Otherwise a tile holds 128 rows of one
+// kv head and 128 keys.
+//
+// Roles (256 threads): warp 0 lane 0 issues TMA (Q once per item, K and V per
+// key tile, two stages); warp 1 allocates TMEM and lane 0 issues the MMAs
+// (S = Q K^T into one of two S buffers, O += P V); warps 4-7 (one row per
+// thread) read S from TMEM, apply the prefix-length / ancestor mask, keep the
+// online softmax in the log2 domain (O is rescaled in TMEM only when the row
+// maximum grows by more than 2^8), write P (bf16) to shared memory and finally
+// normalise O and store the output.  Every wait is bounded: a timeout sets
+// MEDUSA_DEV_TIMEOUT, all roles stop, outstanding copies and MMAs are waited
+// for and TMEM is freed before the kernel returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "sm100.cuh"
+
+namespace medusa {
+using namespace sm100;
+
+namespace tc {
+
+constexpr int kThreads = 256;
+constexpr int kStages = 2;
+constexpr uint32_t kHalf = 16384;                       // 128 rows x 128 bytes
+constexpr uint32_t kBox = 8192;                         // 64 rows x 128 bytes
+constexpr uint32_t kOffQ = 0;                           // 2 d-halves
+constexpr uint32_t kOffStage = 2 * kHalf;               // K (2 halves) + V (2 halves) per stage
+constexpr uint32_t kStageBytes = 4 * kHalf;
+constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // 2 key-halves
+constexpr uint32_t kOffBar = kOffP + 2 * kHalf;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;                     // S0, S1 (128 each), O (128)
+constexpr uint32_t kColO = 256;
+constexpr uint64_t kWaitNs = 1000000000ull;             // 1 s per wait
+constexpr uint64_t kDrainNs = 100000000ull;             // 100 ms per drain wait
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
+
+struct Params {
+  const uint32_t* mask;
+  const int32_t* prefix_len;
+  uint16_t* out;
+  int32_t* d_status;
+  int nl, B, N, Hq, Hkv, G, Lmax, W;
+  int packed;    // two kv heads per tile
+  int mtiles;    // row tiles per head group
+  int groups;    // head groups per (layer, row)
+  int items;
+  int KT;        // key positions per tile: 64 packed, 128 otherwise
+  float scale_log2;
+};
+
+struct Bars {
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, o_done, o_free, drain;
+};
+
+struct Item {
+  int lb, b, h0, mt, L, T, n_pre;
+  bool ok;
+};
+
+// Every lane of the warp waits; the warp continues only if all lanes saw the
+// phase complete (keeps warp-collective tcgen05 operations convergent).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, kWaitNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero): relative error ~2^-22,
+// far below the bf16 rounding P receives next.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ Item decode(const Params& p, int it) {
+  Item x;
+  x.mt = it % p.mtiles;
+  int r = it / p.mtiles;
+  const int grp = r % p.groups;
+  x.lb = r / p.groups;
+  x.b = x.lb % p.B;
+  x.h0 = p.packed ? 2 * grp : grp;
+  x.L = p.prefix_len[x.b];
+  x.ok = x.L >= 0 && x.L <= p.Lmax;
+  x.n_pre = x.ok ? (x.L + p.KT - 1) / p.KT : 0;
+  x.T = x.n_pre + (p.N + p.KT - 1) / p.KT;
+  return x;
+}
+
+}  // namespace tc
+
+template <bool PACKED>
+__global__ void __launch_bounds__(tc::kThreads, 1)
+tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                    const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
+                    const __grid_constant__ CUtensorMap tm_vt, const tc::Params p) {
+  using namespace tc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 128);
+    }
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_free, 128);
+    mbar_init(&bars->drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tm_q);
+    tma_prefetch(&tm_kc);
+    tma_prefetch(&tm_vc);
+    tma_prefetch(&tm_kt);
+    tma_prefetch(&tm_vt);
+  }
+  // Packed tiles: each row's P columns outside its own head block stay zero.
+  if (PACKED && warp >= 4) {
+    const int m = threadIdx.x - 128, other = 1 - (m >> 6);
+    uint4 z = make_uint4(0, 0, 0, 0);
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(smem + kOffP + other * kHalf + m * 128 + c * 16) = z;
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int g = 0, n = 0;
+      bool alive = true;
+      for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
+        const Item x = decode(p, it);
+        if (!x.ok) continue;
+        if (n > 0 && !(alive = mbar_wait_bounded(&bars->q_empty, (n - 1) & 1, &s_abort, kWaitNs))) break;
+        ++n;  // Q loads of item n-1 (0-based) issued below
+        mbar_expect_tx(&bars->q_full, 2 * kHalf);
+        for (int dh = 0; dh < 2; ++dh) {
+          if (PACKED) {
+            for (int s = 0; s < 2; ++s)
+              tma_load_5d(smem + kOffQ + dh * kHalf + s * kBox, &tm_q, &bars->q_full, 64 * dh, 0, x.h0 + s, 0, x.lb);
+          } else {
+            tma_load_5d(smem + kOffQ + dh * kHalf, &tm_q, &bars->q_full, 64 * dh, 0, x.h0, x.mt * (128 / p.G), x.lb);
+          }
+        }
+        for (int t = 0; t < x.T; ++t, ++g) {
+          const int st = g % kStages;
+          if (g >= kStages &&
+              !(alive = mbar_wait_bounded(&bars->kv_empty[st], ((g / kStages) - 1) & 1, &s_abort, kWaitNs)))
+            break;
+          const bool tree = t >= x.n_pre;
+          const int j0 = (tree ? t - x.n_pre : t) * p.KT;
+          const CUtensorMap* mk = tree ? &tm_kt : &tm_kc;
+          const CUtensorMap* mv = tree ? &tm_vt : &tm_vc;
+          uint8_t* kb = smem + kOffStage + st * kStageBytes;
+          uint8_t* vb = kb + 2 * kHalf;
+          mbar_expect_tx(&bars->k_full[st], 2 * kHalf);
+          for (int dh = 0; dh < 2; ++dh)
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_4d(kb + dh * kHalf + cb * kBox, mk, &bars->k_full[st], 64 * dh,
+                          PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
+          mbar_expect_tx(&bars->v_full[st], 2 * kHalf);
+          for (int dh = 0; dh < 2; ++dh)
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_4d(vb + dh * kHalf + cb * kBox, mv, &bars->v_full[st], 64 * dh,
+                          PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
+        }
+      }
+      if (!alive) {
+        // Drain: wait (bounded, regardless of the abort flag) for the last
+        // phase issued on every load barrier, so no copy lands after exit.
+        if (n > 0) mbar_wait_bounded(&bars->q_full, (n - 1) & 1, nullptr, kDrainNs);
+        for (int k = g - 1; k >= 0 && k >= g - kStages; --k) {
+          mbar_wait_bounded(&bars->k_full[k % kStages], (k / kStages) & 1, nullptr, kDrainNs);
+          mbar_wait_bounded(&bars->v_full[k % kStages], (k / kStages) & 1, nullptr, kDrainNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int g = 0, n = 0, pv = 0;
+    bool alive = true;
+    for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
+      const Item x = decode(p, it);
+      if (!x.ok) {
+        if (lane == 0 && x.mt == 0) set_status(p.d_status, MEDUSA_DEV_BAD_LENGTH);
+        continue;
+      }
+      if (!(alive = warp_wait(&bars->q_full, n & 1, &s_abort))) break;
+      tc_fence_after();
+      const int g0 = g;
+      for (int j = 0; j <= x.T && alive; ++j) {
+        if (j < x.T) {
+          const int gj = g0 + j, st = gj % kStages, sb = gj & 1;
+          if (!(alive = warp_wait(&bars->k_full[st], (gj / kStages) & 1, &s_abort))) break;
+          if (gj >= 2 && !(alive = warp_wait(&bars->s_free[sb], ((gj >> 1) - 1) & 1, &s_abort))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t qa = smem_u32(smem + kOffQ);
+            const uint32_t ka = smem_u32(smem + kOffStage + st * kStageBytes);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+              mma_bf16(tmem + sb * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                       kIdescQK, kk > 0);
+            }
+            mma_commit(&bars->s_full[sb]);
+            if (j == x.T - 1) mma_commit(&bars->q_empty);
+          }
+          __syncwarp();
+        }
+        if (j >= 1) {
+          const int t = j - 1, gt = g0 + t, st = gt % kStages;
+          if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
+          if (!(alive = warp_wait(&bars->p_full, pv & 1, &s_abort))) break;
+          if (!(alive = warp_wait(&bars->v_full[st], (gt / kStages) & 1, &s_abort))) break;
+          uint8_t* vb = smem + kOffStage + st * kStageBytes + 2 * kHalf;
+          // The last prefix tile may run past prefix_len: zero those V rows
+          // (stale cache rows may hold anything, and 0 * NaN is NaN).
+          const int j0 = t * p.KT;
+          if (t < x.n_pre && j0 + p.KT > x.L) {
+            const int first = x.L - j0;  // first invalid key offset within a column block / tile
+            for (int idx = lane; idx < 2 * 128 * 8; idx += 32) {
+              const int dh = idx >> 10, r = (idx >> 3) & 127, c = idx & 7;
+              const int off = PACKED ? (r & 63) : r;
+              if (off >= first)
+                *reinterpret_cast<uint4*>(vb + dh * kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t pa = smem_u32(smem + kOffP);
+            const uint32_t va = smem_u32(vb);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              mma_bf16(tmem + kColO, smem_desc_sw128(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, (kk > 0 || t > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->o_done);
+            mma_commit(&bars->kv_empty[st]);
+          }
+          __syncwarp();
+          ++pv;
+        }
+      }
+      g = g0 + x.T;
+      ++n;
+    }
+    if (!alive && lane == 0) {
+      mma_commit(&bars->drain);
+      mbar_wait_bounded(&bars->drain, 0, nullptr, kDrainNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int q4 = warp - 4, m = threadIdx.x - 128;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
+    const int slot = PACKED ? (m >> 6) : 0;          // warp-uniform
+    constexpr int ncol = PACKED ? 64 : 128;
+    const int col0 = PACKED ? 64 * slot : 0;
+    int g = 0, pv = 0;
+    bool alive = true;
+    for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
+      const Item x = decode(p, it);
+      if (!x.ok) continue;
+      // This thread's query row.
+      int r, h;
+      if (PACKED) { r = m & 63; h = x.h0 + slot; }
+      else { r = x.mt * 128 + m; h = x.h0; }
+      const int node = r / p.G, gq = r % p.G;
+      const bool row_ok = node < p.N && h < p.Hkv;
+      float m_used = -INFINITY, l = 0.f;
+      for (int t = 0; t < x.T; ++t, ++g) {
+        const int sb = g & 1;
+        if (!(alive = warp_wait(&bars->s_full[sb], (g >> 1) & 1, &s_abort))) break;
+        tc_fence_after();
+        float s[ncol];
+        tmem_ld32(lane_addr + sb * 128 + col0, s);
+        tmem_ld32(lane_addr + sb * 128 + col0 + 32, s + 32);
+        if constexpr (!PACKED) {
+          tmem_ld32(lane_addr + sb * 128 + 64, s + 64);
+          tmem_ld32(lane_addr + sb * 128 + 96, s + 96);
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[sb]);
+
+        const bool tree = t >= x.n_pre;
+        const int j0 = (tree ? t - x.n_pre : t) * p.KT;
+        uint32_t mw[4] = {0u, 0u, 0u, 0u};
+        if (tree && row_ok) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int word = (j0 >> 5) + w;
+            if (w * 32 < ncol && word < p.W) mw[w] = p.mask[(size_t)node * p.W + word];
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < ncol; ++c) {
+          const int j = j0 + c;
+          bool v = row_ok && (tree ? (j < p.N && ((mw[c >> 5] >> (c & 31)) & 1u)) : (j < x.L));
+          s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+        const float m_new = fmaxf(m_used, mx);
+        const bool need = m_new > m_used + 8.f;
+        if (t > 0) {
+          // PV of the previous tile must be done before O is touched or P rewritten.
+          if (!(alive = warp_wait(&bars->o_done, pv & 1, &s_abort))) break;
+          ++pv;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+            const float f = need ? fast_exp2(m_used - m_new) : 1.f;
+            float o[32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              tmem_ld32(lane_addr + kColO + 32 * c4, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= f;
+              tmem_st32(lane_addr + kColO + 32 * c4, o);
+            }
+            tmem_wait_st();
+            l *= f;
+          }
+        }
+        if (need) m_used = m_new;
+        float rs = 0.f;
+        uint8_t* prow = smem + kOffP + m * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < ncol / 8; ++c8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = s[c8 * 8 + 2 * e] == -INFINITY ? 0.f : fast_exp2(s[c8 * 8 + 2 * e] - m_used);
+            const float b2 = s[c8 * 8 + 2 * e + 1] == -INFINITY ? 0.f : fast_exp2(s[c8 * 8 + 2 * e + 1] - m_used);
+            rs += a + b2;
+            pk[e] = pack_bf16x2(a, b2);
+          }
+          const int kc = (col0 >> 6) + (c8 >> 3);  // key half (P region)
+          const int chunk = c8 & 7;
+          *reinterpret_cast<uint4*>(prow + kc * kHalf + ((chunk ^ (m & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        l += rs;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
+      }
+      if (!alive) break;
+      // Epilogue: O / l -> bf16 output row.
+      if (!(alive = warp_wait(&bars->o_done, pv & 1, &s_abort))) break;
+      ++pv;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = p.out + ((((size_t)x.lb * p.N + (row_ok ? node : 0)) * p.Hq) + (size_t)h * p.G + gq) * 128;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float o[32];
+        tmem_ld32(lane_addr + kColO + 32 * c4, o);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              pk[e] = pack_bf16x2(o[q * 8 + 2 * e] * inv, o[q * 8 + 2 * e + 1] * inv);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free);
+    }
+  }
+
+  if (threadIdx.x == 0 || (warp == 1 && lane == 0) || (warp == 4 && lane == 0)) {
+    if (s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                     const cuuint32_t* box) {
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tree_attention_tc_supported(int N, int Hq, int Hkv, int d, int Lmax, const void* q, const void* kc,
+                                 const void* vc, const void* kt, const void* vt, const void* out) {
+  if (d != 128 || Hkv < 1 || Hq % Hkv || N < 1 || N > MEDUSA_MAX_NODES || Lmax < 1) return false;
+  const int G = Hq / Hkv;
+  if (G > 128 || 128 % G) return false;
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(kt) || !aligned16(vt) || !aligned16(out))
+    return false;
+  return encode_fn() != nullptr;
+}
+
+size_t tree_attention_tc_ws_bytes(int, int, int, int, int, int, int) { return 0; }
+
+medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, const void* kt, const void* vt,
+                                const uint32_t* mask, const int32_t* prefix_len, int n_layers, int B, int N,
+                                int Hq, int Hkv, int d, int Lmax, float scale, void* out, void*, size_t,
+                                int32_t* d_status, cudaStream_t s) {
+  (void)d;
+  const int G = Hq / Hkv;
+  tc::Params p;
+  p.mask = mask;
+  p.prefix_len = prefix_len;
+  p.out = static_cast<uint16_t*>(out);
+  p.d_status = d_status;
+  p.nl = n_layers;
+  p.B = B;
+  p.N = N;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.Lmax = Lmax;
+  p.W = (N + 31) / 32;
+  p.packed = N * G <= 64 ? 1 : 0;
+  p.KT = p.packed ? 64 : 128;
+  p.mtiles = p.packed ? 1 : (N * G + 127) / 128;
+  p.groups = p.packed ? (Hkv + 1) / 2 : Hkv;
+  p.items = n_layers * B * p.groups * p.mtiles;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cuuint64_t LB = (cuuint64_t)n_layers * B;
+  const cuuint64_t es = 2;
+  CUtensorMap mq, mkc, mvc, mkt, mvt;
+  {
+    const int rows = p.packed ? 64 : 128;
+    cuuint64_t dims[5] = {128, (cuuint64_t)G, (cuuint64_t)Hkv, (cuuint64_t)N, LB};
+    cuuint64_t str[4] = {128 * es, (cuuint64_t)G * 128 * es, (cuuint64_t)Hq * 128 * es,
+                         (cuuint64_t)N * Hq * 128 * es};
+    cuuint32_t box[5] = {64, (cuuint32_t)G, 1, (cuuint32_t)(rows / G), 1};
+    if (!make_map(&mq, q, 5, dims, str, box)) return MEDUSA_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[4] = {128, (cuuint64_t)Hkv, (cuuint64_t)Lmax, LB};
+    cuuint64_t str[3] = {128 * es, (cuuint64_t)Hkv * 128 * es, (cuuint64_t)Lmax * Hkv * 128 * es};
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    if (!make_map(&mkc, kc, 4, dims, str, box) || !make_map(&mvc, vc, 4, dims, str, box)) return MEDUSA_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[4] = {128, (cuuint64_t)Hkv, (cuuint64_t)N, LB};
+    cuuint64_t str[3] = {128 * es, (cuuint64_t)Hkv * 128 * es, (cuuint64_t)N * Hkv * 128 * es};
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    if (!make_map(&mkt, kt, 4, dims, str, box) || !make_map(&mvt, vt, 4, dims, str, box)) return MEDUSA_ERR_CUDA;
+  }
+  auto kern = p.packed ? tree_attn_tc_kernel<true> : tree_attn_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  int grid = device_sm_count();
+  if (grid > p.items) grid = p.items;
+  kern<<<grid, tc::kThreads, tc::kSmemBytes, s>>>(mq, mkc, mvc, mkt, mvt, p);
+  return launch_status();
+}
+
+}  // namespace medusa

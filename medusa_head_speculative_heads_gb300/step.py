@@ -1,0 +1,88 @@
+"""One Medusa verify step through the C ABI: the five calls chained on one
+stream with device-resident outputs and workspaces (torch allocates them; the
+library computes everything).
+
+    heads -> tree_build -> tree_attention -> typical_accept -> kv_compact
+
+The backbone between tree_build and tree_attention (embedding, QKV
+projections, RoPE at the tree positions) and between tree_attention and
+typical_accept (output projection, MLP, LM head) is not part of this library:
+the caller supplies the verify pass's q / tree k,v and the base logits at the
+tree nodes.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B_
+
+
+class VerifyStep:
+    def __init__(self, *, B, H, V, K, topk, nl, Hq, Hkv, d, Lmax, dtype, topology, temperature, eps, delta,
+                 device="cuda"):
+        self.dims = dict(B=B, H=H, V=V, K=K, topk=topk, nl=nl, Hq=Hq, Hkv=Hkv, d=d, Lmax=Lmax)
+        self.T, self.eps, self.delta = float(temperature), float(eps), float(delta)
+        self.dtype = dtype
+        self.topo = topology if isinstance(topology, B_.DevTopology) else topology.upload(device)
+        N = self.topo.n_nodes
+        self.N = N
+        i32 = dict(dtype=torch.int32, device=device)
+        self.topk_idx = torch.empty((B, K, topk), **i32)
+        self.topk_logit = torch.empty((B, K, topk), dtype=torch.float32, device=device)
+        self.tokens = torch.empty((B, N), **i32)
+        self.pos = torch.empty((B, N), **i32)
+        self.mask = torch.empty((N, (N + 31) // 32), **i32)
+        self.attn_out = torch.empty((nl, B, N, Hq, d), dtype=dtype, device=device)
+        self.accept_len = torch.empty(B, **i32)
+        self.path_nodes = torch.empty((B, self.topo.max_depth + 1), **i32)
+        self.next_tok = torch.empty(B, **i32)
+        self.new_len = torch.empty(B, **i32)
+        self.status = torch.zeros(1, **i32)
+        L = B_.lib()
+        dt = B_.MEDUSA_BF16 if dtype == torch.bfloat16 else B_.MEDUSA_F32
+        self.ws_heads = B_._ws(L.medusa_heads_workspace_size(B, H, V, K, topk), device)
+        self.ws_attn = B_._ws(L.medusa_tree_attention_workspace_size(nl, B, N, Hq, Hkv, d, Lmax, dt), device)
+        self.ws_acc = B_._ws(L.medusa_typical_accept_workspace_size(B, N), device)
+        # the tensor-core attention path reports a workspace for its split-KV partials
+        self.attn_launches = 1 if self.ws_attn is None else 2
+
+    def heads(self, h, w1, w2, stream=None):
+        B_.medusa_heads(h, w1, w2, self.dims["topk"], self.topk_idx, self.topk_logit, ws=self.ws_heads,
+                        d_status=self.status, stream=stream)
+
+    def tree(self, root_tok, prefix_len, stream=None):
+        B_.medusa_tree_build(self.topo, root_tok, self.topk_idx, prefix_len, self.tokens, self.pos, self.mask,
+                             d_status=self.status, stream=stream)
+
+    def attention(self, q, kc, vc, kt, vt, prefix_len, stream=None):
+        B_.medusa_tree_attention(q, kc, vc, kt, vt, self.mask, prefix_len, out=self.attn_out, ws=self.ws_attn,
+                                 d_status=self.status, stream=stream)
+
+    def accept(self, logits, stream=None):
+        B_.medusa_typical_accept(logits, self.tokens, self.topo, self.T, self.eps, self.delta, self.accept_len,
+                                 self.path_nodes, self.next_tok, ws=self.ws_acc, d_status=self.status,
+                                 stream=stream)
+
+    def compact(self, kc, vc, kt, vt, prefix_len, stream=None):
+        B_.medusa_kv_compact(kc, vc, kt, vt, self.path_nodes, self.accept_len, prefix_len, self.new_len,
+                             d_status=self.status, stream=stream)
+
+    def run(self, h, w1, w2, root_tok, prefix_len, q, kc, vc, kt, vt, logits, stream=None):
+        """The whole verify step (five calls, no host synchronisation)."""
+        self.heads(h, w1, w2, stream)
+        self.tree(root_tok, prefix_len, stream)
+        self.attention(q, kc, vc, kt, vt, prefix_len, stream)
+        self.accept(logits, stream)
+        self.compact(kc, vc, kt, vt, prefix_len, stream)
+
+    def launches_per_step(self) -> int:
+        """Kernels the five calls launch (mirrors the library's dispatch)."""
+        B, V = self.dims["B"], self.dims["V"]
+        passes = -(-B // 8)
+        chunks = min(64, max(1, -(-V // 2048)))
+        heads = 2 * passes + (1 if chunks == 1 else 2)
+        attn = self.attn_launches
+        return heads + 1 + attn + 2 + 2
+
+    def check(self, stream=None) -> int:
+        return B_.medusa_status_check(self.status, stream)

@@ -1,0 +1,121 @@
+"""CPU tests of the C ABI: the library loads, exports every declared symbol,
+its host-side topology builders agree with the oracle's, and host validation
+rejects bad arguments before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import medusa_head_speculative_heads_gb300 as mg
+from medusa_head_speculative_heads_gb300 import binding
+from oracle import topology as otopo
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mg.build()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(medusa_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(mg.lib_path())
+    declared = _declared_functions()
+    assert len(declared) >= 18
+    for name in declared:
+        assert hasattr(L, name), name
+    assert set(declared) == set(binding.EXPORTS)
+    assert mg.medusa_version() == 100
+
+
+def _same_topology(lib_t, orc_t):
+    assert lib_t.n_nodes == orc_t.n_nodes
+    np.testing.assert_array_equal(lib_t.parent, orc_t.parent)
+    np.testing.assert_array_equal(lib_t.depth, orc_t.depth)
+    np.testing.assert_array_equal(lib_t.rank, orc_t.rank)
+    assert lib_t.max_depth == orc_t.max_depth
+    assert lib_t.max_rank == (int(orc_t.rank.max()) + 1 if orc_t.n_nodes > 1 else 0)
+    np.testing.assert_array_equal(lib_t.retrieve, orc_t.retrieve())
+
+
+@pytest.mark.parametrize("spec", [[2, 2], [2, 2, 2, 2], [3, 3, 3, 3], [1, 1, 1, 1, 1], [4, 4, 4, 4], [10, 10]])
+def test_dense_topology_matches_oracle(spec):
+    for cap in (256, 7, 64):
+        _same_topology(mg.Topology.dense(spec, cap), otopo.dense(spec, cap))
+
+
+@pytest.mark.parametrize("paths", [
+    [[0], [0, 0], [0, 1], [0, 0, 0]],
+    [[0], [0, 0], [0, 1], [0, 0, 0], [0, 0, 1], [0, 1, 0], [0, 1, 1]],
+    [[1], [0], [2], [1, 3], [0, 0], [0, 0], [2, 0, 5], [2, 0]],
+    [],
+])
+def test_path_topology_matches_oracle(paths):
+    _same_topology(mg.Topology.from_paths(paths), otopo.from_paths(paths))
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 30, 64, 100, 256])
+def test_greedy_topology_matches_oracle(n):
+    acc = otopo.synthetic_accuracy(4, 10)
+    _same_topology(mg.Topology.greedy(np.array(acc), n), otopo.greedy(acc, n))
+
+
+def test_greedy_other_table_matches_oracle():
+    g = np.random.default_rng(0)
+    acc = np.sort(g.random((5, 6)), axis=1)[:, ::-1]
+    for n in (10, 40, 120):
+        _same_topology(mg.Topology.greedy(acc, n), otopo.greedy(acc.tolist(), n))
+
+
+def test_topology_rejects_malformed_input():
+    with pytest.raises(mg.MedusaError):
+        mg.Topology.from_paths([[0, 1]])  # parent [0] missing
+    with pytest.raises(mg.MedusaError):
+        mg.Topology.from_paths([[-1]])
+    with pytest.raises(mg.MedusaError):
+        mg.Topology.from_paths([[0]] + [[0] * i for i in range(2, 19)])  # deeper than 16
+    with pytest.raises(mg.MedusaError):
+        mg.Topology.dense([2, 2, 2], max_nodes=0)
+    with pytest.raises(mg.MedusaError):
+        mg.Topology.greedy(np.array([[1.5, 0.2]]), 3)
+
+
+def test_host_validation_rejects_before_launch():
+    """Invalid arguments return a status without touching the GPU."""
+    L = mg.lib()
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: validation fails first
+    assert L.medusa_heads(None, fake, fake, 1, 64, 100, 4, 10, 1, fake, fake, None, fake, 1 << 20, None, None) == 1
+    assert L.medusa_heads(fake, fake, fake, 0, 64, 100, 4, 10, 1, fake, fake, None, fake, 1 << 20, None, None) == 1
+    assert L.medusa_heads(fake, fake, fake, 1, 63, 100, 4, 10, 1, fake, fake, None, fake, 1 << 20, None, None) == 1
+    assert L.medusa_heads(fake, fake, fake, 1, 64, 100, 4, 33, 1, fake, fake, None, fake, 1 << 20, None, None) == 1
+    assert L.medusa_heads(fake, fake, fake, 1, 64, 100, 4, 10, 1, fake, fake, None, fake, 16, None, None) == 5
+    assert L.medusa_tree_attention(fake, fake, fake, fake, fake, fake, fake, 1, 1, 300, 4, 4, 128, 64,
+                                   ctypes.c_float(0.1), 1, fake, None, 0, None, None) == 1
+    assert L.medusa_tree_attention(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 6, 4, 128, 64,
+                                   ctypes.c_float(0.1), 1, fake, None, 0, None, None) == 1
+    assert L.medusa_tree_attention(fake, fake, fake, fake, fake, fake, fake, 1, 1, 8, 4, 4, 100, 64,
+                                   ctypes.c_float(0.1), 1, fake, None, 0, None, None) == 1
+    # kv_compact: tree buffer inside the cache -> ALIAS
+    base = 1 << 20
+    assert L.medusa_kv_compact(P(base), P(base * 64), P(base + 4096), P(base * 128), fake, fake, fake, fake,
+                               1, 1, 4, 2, 128, 64, 3, 1, None, None) == 3
+    assert L.medusa_kv_compact(P(base), P(base * 64), P(base * 96), P(base * 128), fake, fake, fake, fake,
+                               1, 1, 4, 2, 128, 64, 17, 1, None, None) == 1
+    st = binding.medusa_dev_topology()
+    st.n_nodes = 7
+    assert L.medusa_typical_accept(fake, fake, ctypes.byref(st), 1, 100, ctypes.c_float(0.5), ctypes.c_float(0.1),
+                                   ctypes.c_float(0.3), fake, fake, fake, None, None, fake, 1 << 20, None, None) == 1
+    assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"

@@ -1,0 +1,322 @@
+"""GPU parity: every entry point of the C ABI against the float64 oracle on
+seeded inputs (sizes the oracle finishes in seconds, spanning several tiles
+and a ragged tail).  Integer outputs are bit-exact; floats meet the stated
+tolerance (tests/helpers.py); near-ties of a float-decided integer are flagged,
+not counted."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import topology as otopo
+import workloads as wl
+from tests.helpers import TOL, bf16_to_f64, check_topk, rel_err, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mg():
+    import medusa_head_speculative_heads_gb300 as m
+    m.build()
+    assert torch.cuda.is_available()
+    return m
+
+
+def _status(mg):
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _tau(dtype):
+    if dtype == "f32":
+        return lambda z: 1e-6 * max(1.0, float(np.max(np.abs(z))))
+    return lambda z: 1e-4 * float(np.sqrt(np.mean(z * z)))
+
+
+# ----------------------------------------------------------------------------- heads
+
+@pytest.mark.parametrize("case", [
+    dict(name="tiny"),
+    dict(name="tiny", dtype="bf16", B=3, H=512, V=5000, K=3, topk=10),
+    dict(name="tiny", dtype="f32", B=5, H=264, V=2049, K=4, topk=32),
+    dict(name="tiny", dtype="bf16", B=8, H=1024, V=4099, K=2, topk=1),
+    dict(name="tiny", dtype="bf16", B=11, H=256, V=700, K=2, topk=4),
+])
+def test_heads_parity(mg, case):
+    c = wl.config(**case)
+    h = wl.hidden(c)
+    w1, w2 = wl.head_weights(c)
+    ref = oracle.heads(h, w1, w2, c["topk"])
+    st = _status(mg)
+    z = torch.empty((c["B"], c["K"], c["V"]), dtype=torch.float32, device="cuda")
+    idx, val = mg.medusa_heads(to_dev(h), to_dev(w1), to_dev(w2), c["topk"], logits=z, d_status=st)
+    torch.cuda.synchronize()
+    assert rel_err(to_host(z), ref["z"]) <= TOL[c["dtype"]]
+    checked, flagged = check_topk(to_host(idx), to_host(val), ref["z"], _tau(c["dtype"]), TOL[c["dtype"]])
+    assert flagged <= max(1, checked // 50)
+    assert mg.medusa_status_check(st) == 0
+    # without the optional logits output (workspace path) the result is identical
+    idx2, val2 = mg.medusa_heads(to_dev(h), to_dev(w1), to_dev(w2), c["topk"])
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2) and torch.equal(val, val2)
+
+
+def test_heads_zero_w1_reproduces_lm_head(mg):
+    """W1 = 0, W2 = LM head: every head returns the base logits' top-k."""
+    c = wl.config("tiny", dtype="bf16", B=2, H=256, V=3000, K=4, topk=10)
+    h = wl.hidden(c)
+    _, w2 = wl.head_weights(c, heads=[0])
+    w2 = np.repeat(w2, 4, 0)
+    w1 = np.zeros((4, 256, 256), np.uint16)
+    z = torch.empty((2, 4, 3000), dtype=torch.float32, device="cuda")
+    idx, _ = mg.medusa_heads(to_dev(h), to_dev(w1), to_dev(w2), 10, logits=z)
+    base = bf16_to_f64(h) @ bf16_to_f64(w2[0]).T
+    zz = to_host(z)
+    for k in range(4):
+        assert rel_err(zz[:, k], base) <= 1e-5
+        assert torch.equal(idx[:, k], idx[:, 0])
+
+
+@pytest.mark.parametrize("V,topk", [(1000, 1), (1000, 10), (32000, 10), (32000, 32), (100000, 17), (33, 32)])
+def test_head_topk_bit_exact(mg, V, topk):
+    g = np.random.default_rng(V + topk)
+    x = (np.round(g.standard_normal((6, V)) * 8) / 8).astype(np.float32)  # many exact ties
+    ref_idx, ref_val = oracle.topk_f32(x, topk)
+    idx, val = mg.medusa_head_topk(to_dev(x), topk)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(idx), ref_idx)
+    np.testing.assert_array_equal(to_host(val).astype(np.float64), ref_val)
+
+
+# ----------------------------------------------------------------------------- tree build
+
+@pytest.mark.parametrize("kind", ["dense7", "dense256", "greedy64", "choices", "chain", "root_only"])
+def test_tree_build_bit_exact(mg, kind):
+    spec = {"dense7": ("dense", [2, 2]), "dense256": ("dense", [4, 4, 4, 4]), "greedy64": ("greedy", 64),
+            "choices": ("paths", [[0], [0, 0], [0, 1], [0, 0, 0], [0, 0, 1], [0, 1, 0], [0, 1, 1]]),
+            "chain": ("dense", [1] * 16), "root_only": ("paths", [])}[kind]
+    if spec[0] == "dense":
+        lt, ot = mg.Topology.dense(spec[1], 256), otopo.dense(spec[1], 256)
+    elif spec[0] == "greedy":
+        acc = otopo.synthetic_accuracy(4, 10)
+        lt, ot = mg.Topology.greedy(np.array(acc), spec[1]), otopo.greedy(acc, spec[1])
+    else:
+        lt, ot = mg.Topology.from_paths(spec[1]), otopo.from_paths(spec[1])
+    g = np.random.default_rng(3)
+    B, K, topk = 5, max(1, ot.max_depth), 10
+    topk_idx = g.integers(0, 32000, (B, K, topk)).astype(np.int32)
+    root = g.integers(0, 32000, B).astype(np.int32)
+    pl = np.array([0, 1, 1023, 4096, 77], np.int32)
+    tokens, pos, mask = otopo.tree_build(ot, root, topk_idx, pl)
+    dt = lt.upload()
+    st = _status(mg)
+    gt, gp, gm = mg.medusa_tree_build(dt, to_dev(root), to_dev(topk_idx), to_dev(pl), d_status=st)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(gt), tokens)
+    np.testing.assert_array_equal(to_host(gp), pos)
+    np.testing.assert_array_equal(to_host(gm).view(np.uint32), mask)
+    assert mg.medusa_status_check(st) == 0
+
+
+# ----------------------------------------------------------------------------- tree attention
+
+ATTN_CASES = [
+    dict(name="tiny"),  # the tiny fp32 configuration: N=7, G=2, d=64, L=128
+    dict(name="tiny", dtype="bf16", nl=2, B=3, Hq=4, Hkv=4, d=128, L=300, tree=("dense", (2, 2, 2), 15),
+         Ls=[300, 0, 129]),
+    dict(name="tiny", dtype="bf16", nl=1, B=2, Hq=8, Hkv=2, d=128, L=200, tree=("greedy", 10, 64), Ls=[200, 65]),
+    dict(name="tiny", dtype="f32", nl=2, B=2, Hq=6, Hkv=3, d=96, L=70, tree=("dense", (3, 3), 13), Ls=[70, 33]),
+    dict(name="tiny", dtype="bf16", nl=1, B=1, Hq=2, Hkv=1, d=64, L=40, tree=("paths", []), Ls=[40]),
+    dict(name="tiny", dtype="bf16", nl=1, B=2, Hq=2, Hkv=2, d=128, L=130, tree=("dense", (4, 4, 4, 4), 256),
+         Ls=[130, 1]),
+    # tensor-core path: two kv heads per tile, odd kv-head count, prefix an exact tile multiple
+    dict(name="tiny", dtype="bf16", nl=1, B=2, Hq=6, Hkv=3, d=128, L=100, tree=("dense", (2, 2, 2), 15),
+         Ls=[100, 64]),
+    # GQA group of 2 with 64 nodes: 128 rows per tile, empty prefix
+    dict(name="tiny", dtype="bf16", nl=2, B=1, Hq=4, Hkv=2, d=128, L=20, tree=("greedy", 10, 64), Ls=[0]),
+    # a single node (plain decode) on one kv head
+    dict(name="tiny", dtype="bf16", nl=1, B=1, Hq=1, Hkv=1, d=128, L=5, tree=("paths", []), Ls=[5]),
+    # GQA group of 8 packed two heads per tile
+    dict(name="tiny", dtype="bf16", nl=1, B=3, Hq=16, Hkv=2, d=128, L=130, tree=("dense", (2, 2), 7),
+         Ls=[130, 1, 63]),
+    # more work items than SMs: every CTA runs several items through the pipeline
+    dict(name="tiny", dtype="bf16", nl=4, B=2, Hq=40, Hkv=40, d=128, L=200, tree=("greedy", 10, 64),
+         Ls=[200, 64]),
+]
+
+
+def _topo(c):
+    kind = c["tree"][0]
+    if kind == "dense":
+        return otopo.dense(list(c["tree"][1]), c["tree"][2])
+    if kind == "greedy":
+        return otopo.greedy(otopo.synthetic_accuracy(4, c["tree"][1]), c["tree"][2])
+    return otopo.from_paths(c["tree"][1])
+
+
+@pytest.mark.parametrize("case", ATTN_CASES,
+                         ids=lambda c: f"{c.get('dtype', 'f32')}-d{c.get('d', 64)}-Hq{c.get('Hq', 4)}-Hkv{c.get('Hkv', 2)}"
+                                       f"-nl{c.get('nl', 1)}-B{c.get('B', 1)}-{c.get('tree', ('dense',))[0]}")
+def test_tree_attention_parity(mg, case):
+    c = wl.config(**{k: v for k, v in case.items() if k != "Ls"})
+    t = _topo(c)
+    N = t.n_nodes
+    pl = np.array(case.get("Ls", [c["L"]] * c["B"]), np.int32)
+    q = wl.queries(c, N)
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    _, _, mask = otopo.tree_build(t, np.zeros(c["B"], np.int32), np.zeros((c["B"], max(1, t.max_depth), 10), np.int32), pl)
+    ref = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    st = _status(mg)
+    out = mg.medusa_tree_attention(to_dev(q), to_dev(kc), to_dev(vc), to_dev(kt), to_dev(vt),
+                                   to_dev(mask.view(np.int32)), to_dev(pl), d_status=st)
+    torch.cuda.synchronize()
+    o = to_host(out)
+    o = bf16_to_f64(o) if c["dtype"] == "bf16" else o
+    assert rel_err(o, ref) <= TOL[c["dtype"]]
+    assert mg.medusa_status_check(st) == 0
+
+
+def test_tree_attention_ignores_rows_past_prefix(mg):
+    """NaN in every cache row at and past prefix_len must not reach the output."""
+    c = wl.config("tiny", dtype="bf16", nl=1, B=2, Hq=4, Hkv=4, d=128, L=100)
+    t = otopo.dense([2, 2, 2])
+    N = t.n_nodes
+    pl = np.array([100, 37], np.int32)
+    q = wl.queries(c, N)
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    for b in range(2):
+        kc[:, b, pl[b]:] = 0x7FC0
+        vc[:, b, pl[b]:] = 0x7FC0
+    _, _, mask = otopo.tree_build(t, np.zeros(2, np.int32), np.zeros((2, 3, 10), np.int32), pl)
+    ref = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    out = mg.medusa_tree_attention(to_dev(q), to_dev(kc), to_dev(vc), to_dev(kt), to_dev(vt),
+                                   to_dev(mask.view(np.int32)), to_dev(pl))
+    torch.cuda.synchronize()
+    o = bf16_to_f64(to_host(out))
+    assert np.all(np.isfinite(o))
+    assert rel_err(o, ref) <= TOL["bf16"]
+
+
+def test_tree_attention_bad_prefix_len_reports(mg):
+    c = wl.config("tiny", nl=1, B=1, Hq=2, Hkv=2, d=64, L=16)
+    t = otopo.dense([2])
+    q = wl.queries(c, 3)
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, 3)
+    mask = np.array([[1], [3], [5]], np.uint32)
+    st = _status(mg)
+    mg.medusa_tree_attention(to_dev(q), to_dev(kc), to_dev(vc), to_dev(kt), to_dev(vt), to_dev(mask.view(np.int32)),
+                             to_dev(np.array([c["Lmax"] + 1], np.int32)), d_status=st)
+    assert mg.medusa_status_check(st) == 5  # BAD_LENGTH
+
+
+# ----------------------------------------------------------------------------- typical acceptance
+
+def _accept_case(mg, c, t, tokens, logits, T, eps, delta):
+    ref = oracle.typical_accept(logits, tokens, t.parent, T, eps, delta, Dmax=t.max_depth)
+    lt = mg.Topology.from_paths([list(p) for p in t.paths[1:]])
+    dt = lt.upload()
+    st = _status(mg)
+    al, pn, nt, pt, th = mg.medusa_typical_accept(to_dev(logits), to_dev(tokens), dt, T, eps, delta, d_status=st,
+                                                  want_probs=True)
+    torch.cuda.synchronize()
+    assert mg.medusa_status_check(st) == 0
+    al, pn, nt, pt, th = (to_host(x) for x in (al, pn, nt, pt, th))
+    flagged_rows = 0
+    for b in range(tokens.shape[0]):
+        near = np.abs(ref["p_tok"][b, 1:] - ref["thr"][b, 1:]) < 1e-6 if T > 0 else np.zeros(t.n_nodes - 1, bool)
+        if near.any():
+            # within 1e-6 of the threshold: flagged, not counted; the result must still be a valid path
+            agree = al[b] == ref["accept_len"][b] and np.array_equal(pn[b], ref["path_nodes"][b])
+            flagged_rows += 0 if agree else 1
+            assert 1 <= al[b] <= t.max_depth + 1
+            continue
+        assert al[b] == ref["accept_len"][b]
+        np.testing.assert_array_equal(pn[b], ref["path_nodes"][b])
+        assert nt[b] == ref["next_tok"][b]
+    assert np.max(np.abs(pt - ref["p_tok"])) <= 1e-5
+    assert rel_err(th[:, 1:], ref["thr"][:, 1:]) <= 1e-4
+    return ref, flagged_rows
+
+
+@pytest.mark.parametrize("T,eps,delta,prob", [(0.0, 0.09, 0.3, 0.6), (0.7, 0.09, 0.3, 0.6), (1.0, 0.25, 0.5, 0.5),
+                                              (0.3, 0.09, 0.3, 0.9), (2.0, 0.0, 0.3, 0.1)])
+def test_typical_accept_parity(mg, T, eps, delta, prob):
+    c = wl.config("tiny", V=32000, B=6)
+    t = otopo.greedy(otopo.synthetic_accuracy(4, 10), 64)
+    tokens = wl.random_tokens(c, t.n_nodes)
+    logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=prob)
+    ref, flagged = _accept_case(mg, c, t, tokens, logits, T, eps, delta)
+    assert flagged <= 1
+
+
+def test_typical_accept_tiny_config_and_dense_tree(mg):
+    c = wl.config("tiny")
+    t = otopo.dense([2, 2])
+    tokens = wl.random_tokens(c, t.n_nodes)
+    logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=1.0)
+    ref, _ = _accept_case(mg, c, t, tokens, logits, 0.0, c["eps"], c["delta"])
+    assert ref["accept_len"][0] == 3  # planted with probability 1 along first children
+    t = otopo.dense([4, 4, 4, 4], 256)
+    c = wl.config("tiny", V=3001, B=3)
+    tokens = wl.random_tokens(c, t.n_nodes)
+    logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=0.8)
+    _accept_case(mg, c, t, tokens, logits, 0.8, 0.09, 0.3)
+
+
+def test_typical_accept_bad_token_reports(mg):
+    c = wl.config("tiny", V=100, B=1)
+    t = otopo.dense([2])
+    tokens = np.array([[5, 100, 3]], np.int32)
+    logits = wl.base_logits(c, 3)
+    dt = mg.Topology.dense([2]).upload()
+    st = _status(mg)
+    al, *_ = mg.medusa_typical_accept(to_dev(logits), to_dev(tokens), dt, 0.5, 0.09, 0.3, d_status=st)
+    assert mg.medusa_status_check(st) == 1  # BAD_INDEX
+    assert int(al[0]) in (1, 2)
+
+
+# ----------------------------------------------------------------------------- kv compaction
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_kv_compact_bit_exact(mg, dtype):
+    c = wl.config("tiny", dtype=dtype, nl=3, B=4, Hkv=2, d=64, L=50)
+    t = otopo.dense([2, 2, 2])
+    N = t.n_nodes
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    Lmax = kc.shape[2]
+    pl = np.array([50, 0, Lmax - 2, 17], np.int32)  # row 2 overflows with accept_len 4
+    path = np.array([[0, 1, 3, 7], [0, 2, -1, -1], [0, 1, 4, 10], [0, -1, -1, -1]], np.int32)
+    acc = np.array([4, 2, 4, 1], np.int32)
+    rk, rv, rlen, rovf = oracle.kv_compact(kc, vc, kt, vt, path, acc, pl)
+    dkc, dvc = to_dev(kc), to_dev(vc)
+    st = _status(mg)
+    dpl = to_dev(pl)
+    new_len = mg.medusa_kv_compact(dkc, dvc, to_dev(kt), to_dev(vt), to_dev(path), to_dev(acc), dpl,
+                                   new_len=dpl, d_status=st)  # new_len aliases prefix_len
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(dkc), rk)
+    np.testing.assert_array_equal(to_host(dvc), rv)
+    np.testing.assert_array_equal(to_host(new_len), rlen)
+    assert mg.medusa_status_check(st) == 2  # CACHE_OVERFLOW (row 2)
+
+
+# ----------------------------------------------------------------------------- one whole step
+
+def test_full_step_tiny_config(mg):
+    """The tiny fp32 configuration through all five calls, chained on one stream."""
+    from tests.step import run_gpu_step, run_oracle_step, make_step_inputs
+    c = wl.config("tiny")
+    inp = make_step_inputs(c)
+    ref = run_oracle_step(c, inp)
+    got = run_gpu_step(mg, c, inp)
+    for key in ("topk_idx", "tokens", "pos", "mask", "accept_len", "path_nodes", "next_tok", "new_len"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    assert rel_err(got["attn_out"], ref["attn_out"]) <= TOL["f32"]
+    np.testing.assert_array_equal(got["kc"], ref["kc"])
+    np.testing.assert_array_equal(got["vc"], ref["vc"])

@@ -165,3 +165,20 @@ def plant(c, logits, tokens, parent, prob=None, rows=None, margin: float = 4.0) 
                 continue
             out[i, n, tokens[i, ch]] = out[i, n].max() + np.float32(margin)
     return out
+
+
+def step_inputs(c: dict, N: int, layers=None, rows=None) -> dict:
+    """Every synthetic input of one verify step except the planted logits.
+
+    Weights, hidden states, root tokens and prefix lengths; the backbone's
+    verify-pass q/k/v at the tree nodes and the prefix cache; unplanted base
+    logits at the tree nodes.  `layers` / `rows` restrict the per-layer and
+    per-row tensors to a subset (same values as in the full tensors).
+    """
+    rows_l = list(range(c["B"])) if rows is None else list(rows)
+    w1, w2 = head_weights(c)
+    kc, vc = kv_cache(c, layers, rows_l)
+    kt, vt = tree_kv(c, N, layers, rows_l)
+    return dict(h=hidden(c, rows_l), w1=w1, w2=w2, root_tok=root_tokens(c, rows_l),
+                prefix_len=np.full(len(rows_l), c["L"], np.int32), q=queries(c, N, layers, rows_l),
+                kc=kc, vc=vc, kt=kt, vt=vt, logits=base_logits(c, N, rows_l), rows=rows_l)
