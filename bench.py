@@ -177,9 +177,18 @@ def run_ours(args, c):
         print(f"profile {args.profile}: {args.steps} calls done")
         return
 
-    # ---- timed region (device events; per-call events on the launching stream)
+    # The whole step as one CUDA graph (the five calls are stream-ordered with no
+    # host synchronisation, so they capture as they are).
+    graph = vs.capture(d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"],
+                       d["vt"], d["logits"])
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if vs.check() != 0:
+        raise RuntimeError("device status set during graph warm-up")
+
+    # ---- timed region: exactly K steps (graph replays), device events on the stream
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     sampler = ClockSampler(local) if rank == 0 else None
     if world > 1:
         dist.barrier()
@@ -187,6 +196,21 @@ def run_ours(args, c):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
+    for i in range(K):
+        graph.replay()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # ---- per-call breakdown (separate eager pass, events between the calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     for i in range(K):
         e = ev[i]
         e[0].record(stream)
@@ -200,16 +224,7 @@ def run_ours(args, c):
         e[4].record(stream)
         vs.compact(d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"], stream)
         e[5].record(stream)
-    t_end.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop() if sampler else None
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
     names = ["heads", "tree_build", "attention", "accept", "compact"]
     per_call = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j, n in enumerate(names)}
     accept_len = vs.accept_len.float().mean().item()
@@ -277,7 +292,8 @@ def run_e2e(args, c, vs, inp, d, dev, stream):
     its per-step inputs (hidden state, root token, prefix length, the verify
     pass's q and tree k/v, the base logits at the tree nodes) from pinned host
     memory and reads back the step's results (accept length, path, next token,
-    new cache length).  Weights and the KV cache stay resident (model state)."""
+    new cache length); copies and calls are one CUDA graph per step.  Weights
+    and the KV cache stay resident (model state)."""
     import torch
     names = ["h", "root_tok", "prefix_len", "q", "kt", "vt", "logits"]
     host = {}
@@ -289,22 +305,24 @@ def run_e2e(args, c, vs, inp, d, dev, stream):
     h2d = sum(host[k].numel() * host[k].element_size() for k in names)
     d2h = sum(o.numel() * o.element_size() for o in outs)
 
-    def step():
+    def pre():
         for k in names:
             d[k].copy_(host[k], non_blocking=True)
-        vs.run(d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"],
-               d["vt"], d["logits"], stream=stream)
+
+    def post():
         for o, ho in zip(outs, host_out):
             ho.copy_(o, non_blocking=True)
 
+    graph = vs.capture(d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"],
+                       d["vt"], d["logits"], pre=pre, post=post)
     for _ in range(max(3, args.warmup)):
-        step()
+        graph.replay()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        step()
+        graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps

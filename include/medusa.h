@@ -141,8 +141,9 @@ medusa_status medusa_topology_upload(const medusa_topology* t, int32_t* d_buf, s
  *   topk_logit [B][K][topk]  fp32 out
  *   logits_or_null [B][K][V] fp32 out, optional (all head logits z)
  * 1 <= B <= 64, 1 <= K <= MEDUSA_MAX_DEPTH, 1 <= topk <= min(V, MEDUSA_MAX_TOPK),
- * H a multiple of 8, pointers 16-byte aligned.  The workspace holds u, z and
- * the partial top-k lists. */
+ * H a multiple of 8, pointers 16-byte aligned.  The workspace holds u and the
+ * per-CTA candidate lists the W2 pass ranks; z is written only to
+ * logits_or_null. */
 size_t medusa_heads_workspace_size(int B, int H, int V, int K, int topk);
 medusa_status medusa_heads(const void* h, const void* w1, const void* w2, int B, int H, int V,
                            int K, int topk, medusa_dtype dt, int32_t* topk_idx, float* topk_logit,
@@ -219,8 +220,9 @@ medusa_status medusa_tree_attention(const void* q, const void* kc, const void* v
  *   node's token and the parent's threshold (root: 1 and 0), optional.
  *   tokens [B][N] int32 from tree_build; token ids must lie in [0, V) (else
  *   BAD_INDEX and the node fails its test).  temperature >= 0, eps >= 0,
- *   delta >= 0. */
-size_t medusa_typical_accept_workspace_size(int B, int N);
+ *   delta >= 0.  The workspace (16-byte aligned) holds per-chunk partial
+ *   statistics of every node's logit row. */
+size_t medusa_typical_accept_workspace_size(int B, int N, int V);
 medusa_status medusa_typical_accept(const float* logits, const int32_t* tokens,
                                     const medusa_dev_topology* t, int B, int V, float temperature,
                                     float eps, float delta, int32_t* accept_len,

@@ -82,7 +82,7 @@ def lib():
             "medusa_tree_build": (I, [P, P, P, I, I, I, P, P, P, P, P, P]),
             "medusa_tree_attention_workspace_size": (Z, [I, I, I, I, I, I, I, I]),
             "medusa_tree_attention": (I, [P, P, P, P, P, P, P] + [I] * 7 + [F, I, P, P, Z, P, P]),
-            "medusa_typical_accept_workspace_size": (Z, [I, I]),
+            "medusa_typical_accept_workspace_size": (Z, [I, I, I]),
             "medusa_typical_accept": (I, [P, P, P, I, I, F, F, F, P, P, P, P, P, P, Z, P, P]),
             "medusa_kv_compact": (I, [P, P, P, P, P, P, P, P] + [I] * 8 + [P, P]),
             "medusa_status_check": (I, [P, P, P]),
@@ -286,7 +286,7 @@ def medusa_typical_accept(logits, tokens, topo: DevTopology, temperature: float,
         p_tok = torch.empty((B, N), dtype=torch.float32, device=dev)
     if want_probs and thr is None:
         thr = torch.empty((B, N), dtype=torch.float32, device=dev)
-    ws = _ws(lib().medusa_typical_accept_workspace_size(B, N), dev, ws)
+    ws = _ws(lib().medusa_typical_accept_workspace_size(B, N, V), dev, ws)
     _check("medusa_typical_accept", lib().medusa_typical_accept(
         _ptr(logits), _ptr(tokens), ctypes.byref(topo.st), B, V, float(temperature), float(eps), float(delta),
         _ptr(accept_len), _ptr(path_nodes), _ptr(next_tok), _ptr(p_tok), _ptr(thr), _ptr(ws),

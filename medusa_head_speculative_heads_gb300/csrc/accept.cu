@@ -8,13 +8,16 @@
 // at temperature 0 this is greedy decoding.  Skill-pack guide, "树形验证":
 // the longest valid candidate is accepted.
 //
-// Two kernels.  node_stats: one CTA per (node, row) reads the node's fp32
-// logit row once for the argmax and once more (from L2) for the tempered
-// partition function S and E = sum e^((z-m)/T) (z-m)/T, giving
-// H = ln S - E/S; it then tests every child of the node.  select_path: one
-// CTA per row propagates acceptance level by level (a node is accepted iff its
-// parent is and it passed), picks the deepest accepted node (lowest index on
-// ties) and writes the path, its length and the next root token.
+// Two kernels.  node_partial: one CTA per (vocabulary chunk, node, row) reads
+// its slice of the node's fp32 logits once for the max/argmax and once more
+// (from L1/L2) for the tempered sums S_c = sum e^((z-m_c)/T) and
+// E_c = sum e^((z-m_c)/T) (z-m_c)/T.  select_path: one CTA per row combines the
+// chunk partials exactly (S = sum_c S_c e^((m_c-m)/T), E likewise), giving
+// H = ln S - E/S and the threshold per node, tests every child against its
+// parent's distribution, propagates acceptance level by level (a node is
+// accepted iff its parent is and it passed), picks the deepest accepted node
+// (lowest index on ties) and writes the path, its length and the next root
+// token.
 #include <limits.h>
 
 #include "common.cuh"
@@ -22,7 +25,14 @@
 
 namespace medusa {
 
-constexpr int kStatThreads = 256;
+constexpr int kPartThreads = 128;
+constexpr int kChunkValues = 2048;
+constexpr int kMaxChunks = 32;
+
+int accept_chunks(int V) {
+  int c = (V + kChunkValues - 1) / kChunkValues;
+  return c < 1 ? 1 : c > kMaxChunks ? kMaxChunks : c;
+}
 
 __device__ __forceinline__ void block_argmax(float& v, int& i, float* sv, int* si) {
 #pragma unroll
@@ -60,104 +70,75 @@ __device__ __forceinline__ float block_sum(float v, float* s) {
   return r;
 }
 
-// Grid (N, B).  Writes, for every child c of node n: pass[b][c], and the
-// optional p_tok / thr; for node n itself: amax[b][n].
-__global__ void __launch_bounds__(kStatThreads)
-node_stats_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
-                  const int32_t* __restrict__ parent, int N, int V, float T, float eps, float delta,
-                  int32_t* __restrict__ pass, int32_t* __restrict__ amax, float* __restrict__ p_tok,
-                  float* __restrict__ thr_out, int32_t* d_status) {
-  __shared__ float sv[kStatThreads / 32];
-  __shared__ int si[kStatThreads / 32];
-  const int n = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+// Grid (C, N, B).  part[(b*N + n)*C + c] = {max, argmax (bits), S_c, E_c}.
+__global__ void __launch_bounds__(kPartThreads)
+node_partial_kernel(const float* __restrict__ logits, int N, int V, int C, float T, float4* __restrict__ part) {
+  __shared__ float sv[kPartThreads / 32];
+  __shared__ int si[kPartThreads / 32];
+  const int c = blockIdx.x, n = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const float* z = logits + ((size_t)b * N + n) * V;
+  const int cs = ((V + C - 1) / C + 3) & ~3;  // chunk size, a multiple of 4
+  const int lo = c * cs, hi = min(V, lo + cs);
   const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
 
   float mv = -INFINITY;
   int mi = INT_MAX;
   if (vec) {
     const float4* z4 = reinterpret_cast<const float4*>(z);
-    for (int q = tid; q < V / 4; q += kStatThreads) {
-      float4 t = z4[q];
-      float e[4] = {t.x, t.y, t.z, t.w};
+    for (int q = (lo >> 2) + tid; q < (hi >> 2); q += kPartThreads) {
+      const float4 t = z4[q];
+      const float e[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (ranks_ahead(e[j], 4 * q + j, mv, mi)) { mv = e[j]; mi = 4 * q + j; }
     }
   } else {
-    for (int v = tid; v < V; v += kStatThreads)
+    for (int v = lo + tid; v < hi; v += kPartThreads)
       if (ranks_ahead(z[v], v, mv, mi)) { mv = z[v]; mi = v; }
   }
   block_argmax(mv, mi, sv, si);
 
-  float S = 1.f, thr;
-  if (T > 0.f) {
+  float S = 0.f, E = 0.f;
+  if (T > 0.f && lo < hi) {
     const float inv_t = 1.f / T;
     float s = 0.f, e = 0.f;
     if (vec) {
       const float4* z4 = reinterpret_cast<const float4*>(z);
-      for (int q = tid; q < V / 4; q += kStatThreads) {
-        float4 t = z4[q];
-        float x[4] = {t.x, t.y, t.z, t.w};
+      for (int q = (lo >> 2) + tid; q < (hi >> 2); q += kPartThreads) {
+        const float4 t = z4[q];
+        const float x[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float a = (x[j] - mv) * inv_t;
-          float w = expf(a);
+          const float a = (x[j] - mv) * inv_t;
+          const float w = expf(a);
           s += w;
           e = fmaf(w, a, e);
         }
       }
     } else {
-      for (int v = tid; v < V; v += kStatThreads) {
-        float a = (z[v] - mv) * inv_t;
-        float w = expf(a);
+      for (int v = lo + tid; v < hi; v += kPartThreads) {
+        const float a = (z[v] - mv) * inv_t;
+        const float w = expf(a);
         s += w;
         e = fmaf(w, a, e);
       }
     }
     S = block_sum(s, sv);
-    float E = block_sum(e, sv);
-    float H = logf(S) - E / S;
-    thr = fminf(eps, delta * expf(-H));
-  } else {
-    thr = fminf(eps, delta);
+    E = block_sum(e, sv);
   }
-
-  if (tid == 0) amax[(size_t)b * N + n] = mi;
-  if (n == 0 && tid == 0) {
-    pass[(size_t)b * N] = 1;
-    if (p_tok) p_tok[(size_t)b * N] = 1.f;
-    if (thr_out) thr_out[(size_t)b * N] = 0.f;
-  }
-  for (int c = 1 + tid; c < N; c += kStatThreads) {
-    if (parent[c] != n) continue;
-    const int x = tokens[(size_t)b * N + c];
-    int ok;
-    float p;
-    if (x < 0 || x >= V) {
-      set_status(d_status, MEDUSA_DEV_BAD_INDEX);
-      ok = 0;
-      p = 0.f;
-    } else if (T > 0.f) {
-      p = expf((z[x] - mv) / T) / S;
-      ok = p > thr;
-    } else {
-      ok = x == mi;
-      p = ok ? 1.f : 0.f;
-    }
-    pass[(size_t)b * N + c] = ok;
-    if (p_tok) p_tok[(size_t)b * N + c] = p;
-    if (thr_out) thr_out[(size_t)b * N + c] = thr;
-  }
+  if (tid == 0) part[((size_t)b * N + n) * C + c] = make_float4(mv, __int_as_float(mi), S, E);
 }
 
 // Grid B; block = N rounded up to a warp multiple (<= 256).
 __global__ void __launch_bounds__(MEDUSA_MAX_NODES)
-select_path_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int N,
-                   int max_depth, const int32_t* __restrict__ pass, const int32_t* __restrict__ amax,
+select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
+                   const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int N, int V,
+                   int max_depth, int C, float T, float eps, float delta, const float4* __restrict__ part,
                    int32_t* __restrict__ accept_len, int32_t* __restrict__ path_nodes,
-                   int32_t* __restrict__ next_tok, int32_t* d_status) {
-  __shared__ int acc[MEDUSA_MAX_NODES];
+                   int32_t* __restrict__ next_tok, float* __restrict__ p_tok, float* __restrict__ thr_out,
+                   int32_t* d_status) {
+  __shared__ int acc[MEDUSA_MAX_NODES], pass[MEDUSA_MAX_NODES], amax[MEDUSA_MAX_NODES];
+  __shared__ float zmax[MEDUSA_MAX_NODES], ssum[MEDUSA_MAX_NODES], thr[MEDUSA_MAX_NODES];
   __shared__ int s_key[MEDUSA_MAX_NODES / 32];
   __shared__ int s_bad;
   const int b = blockIdx.x, c = threadIdx.x;
@@ -168,6 +149,38 @@ select_path_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
     dc = depth[c];
     pc = parent[c];
     if (c > 0 && (pc < 0 || pc >= c || dc < 1 || dc > max_depth)) s_bad = 1;
+    // Combine this node's chunk partials.
+    const float4* pp = part + ((size_t)b * N + c) * C;
+    float m = -INFINITY;
+    int a = INT_MAX;
+    for (int k = 0; k < C; ++k) {
+      const float4 q = pp[k];
+      const int qi = __float_as_int(q.y);
+      if (ranks_ahead(q.x, qi, m, a)) { m = q.x; a = qi; }
+    }
+    float th;
+    float S = 1.f;
+    if (T > 0.f) {
+      const float inv_t = 1.f / T;
+      float e = 0.f;
+      S = 0.f;
+      for (int k = 0; k < C; ++k) {
+        const float4 q = pp[k];
+        if (q.z == 0.f) continue;  // an empty chunk
+        const float d = (q.x - m) * inv_t;
+        const float w = expf(d);
+        S = fmaf(q.z, w, S);
+        e = fmaf(w, fmaf(q.z, d, q.w), e);
+      }
+      const float H = logf(S) - e / S;
+      th = fminf(eps, delta * expf(-H));
+    } else {
+      th = fminf(eps, delta);
+    }
+    zmax[c] = m;
+    ssum[c] = S;
+    thr[c] = th;
+    amax[c] = a;
     acc[c] = c == 0 ? 1 : 0;
   }
   __syncthreads();
@@ -175,13 +188,37 @@ select_path_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
     if (c == 0) {
       set_status(d_status, MEDUSA_DEV_BAD_TOPOLOGY);
       accept_len[b] = 1;
-      next_tok[b] = amax[(size_t)b * N];
+      next_tok[b] = amax[0];
       for (int j = 0; j <= max_depth; ++j) path_nodes[(size_t)b * (max_depth + 1) + j] = j ? -1 : 0;
     }
     return;
   }
+  // Child tests against the parent's distribution.
+  if (c < N) {
+    int ok = 1;
+    float p = 1.f, t = 0.f;
+    if (c > 0) {
+      const int x = tokens[(size_t)b * N + c];
+      t = thr[pc];
+      if (x < 0 || x >= V) {
+        set_status(d_status, MEDUSA_DEV_BAD_INDEX);
+        ok = 0;
+        p = 0.f;
+      } else if (T > 0.f) {
+        p = expf((logits[((size_t)b * N + pc) * V + x] - zmax[pc]) / T) / ssum[pc];
+        ok = p > t;
+      } else {
+        ok = x == amax[pc];
+        p = ok ? 1.f : 0.f;
+      }
+    }
+    pass[c] = ok;
+    if (p_tok) p_tok[(size_t)b * N + c] = p;
+    if (thr_out) thr_out[(size_t)b * N + c] = t;
+  }
+  __syncthreads();
   for (int d = 1; d <= max_depth; ++d) {
-    if (c < N && dc == d) acc[c] = acc[pc] && pass[(size_t)b * N + c];
+    if (c < N && dc == d) acc[c] = acc[pc] && pass[c];
     __syncthreads();
   }
   // Deepest accepted node, lowest index: maximise key = depth * 512 + (511 - c).
@@ -203,20 +240,44 @@ select_path_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict
       a = j ? parent[a] : -1;
     }
     accept_len[b] = db + 1;
-    next_tok[b] = amax[(size_t)b * N + best];
+    next_tok[b] = amax[best];
   }
+}
+
+// Argument checks shared by the entry points of this file.
+medusa_status typical_accept_check(const float* logits, const int32_t* tokens, const medusa_dev_topology* t, int B,
+                                   int V, float temperature, float eps, float delta, const int32_t* accept_len,
+                                   const int32_t* path_nodes, const int32_t* next_tok) {
+  if (!logits || !tokens || !t || !t->parent || !t->depth || !accept_len || !path_nodes || !next_tok)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || V < 1 || t->n_nodes < 1 || t->n_nodes > MEDUSA_MAX_NODES) return MEDUSA_ERR_INVALID_ARG;
+  if (t->max_depth < 0 || t->max_depth > MEDUSA_MAX_DEPTH) return MEDUSA_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || !(eps >= 0.f) || !(delta >= 0.f)) return MEDUSA_ERR_INVALID_ARG;
+  return MEDUSA_OK;
+}
+
+// Enqueues both kernels with `part` (B * N * accept_chunks(V) float4) as scratch.
+medusa_status typical_accept_launch(const float* logits, const int32_t* tokens, const medusa_dev_topology* t,
+                                    int B, int V, float temperature, float eps, float delta, int32_t* accept_len,
+                                    int32_t* path_nodes, int32_t* next_tok, float* p_tok_or_null,
+                                    float* thr_or_null, float4* part, int32_t* d_status, cudaStream_t s) {
+  const int N = t->n_nodes;
+  const int C = accept_chunks(V);
+  node_partial_kernel<<<dim3(C, N, B), kPartThreads, 0, s>>>(logits, N, V, C, temperature, part);
+  const int threads = (N + 31) / 32 * 32;
+  select_path_kernel<<<B, threads, 0, s>>>(logits, tokens, t->parent, t->depth, N, V, t->max_depth, C, temperature,
+                                           eps, delta, part, accept_len, path_nodes, next_tok, p_tok_or_null,
+                                           thr_or_null, d_status);
+  return launch_status();
 }
 
 }  // namespace medusa
 
 using namespace medusa;
 
-extern "C" size_t medusa_typical_accept_workspace_size(int B, int N) {
-  if (B <= 0 || N <= 0) return 0;
-  WsCarver w(nullptr);
-  w.take<int32_t>((size_t)B * N);
-  w.take<int32_t>((size_t)B * N);
-  return w.used;
+extern "C" size_t medusa_typical_accept_workspace_size(int B, int N, int V) {
+  if (B <= 0 || N <= 0 || V <= 0) return 0;
+  return (size_t)B * N * accept_chunks(V) * sizeof(float4);
 }
 
 extern "C" medusa_status medusa_typical_accept(const float* logits, const int32_t* tokens,
@@ -226,22 +287,13 @@ extern "C" medusa_status medusa_typical_accept(const float* logits, const int32_
                                                int32_t* next_tok, float* p_tok_or_null,
                                                float* thr_or_null, void* ws, size_t ws_bytes,
                                                int32_t* d_status, medusa_stream_t stream) {
-  if (!logits || !tokens || !t || !t->parent || !t->depth || !accept_len || !path_nodes || !next_tok)
-    return MEDUSA_ERR_INVALID_ARG;
-  if (B < 1 || V < 1 || t->n_nodes < 1 || t->n_nodes > MEDUSA_MAX_NODES) return MEDUSA_ERR_INVALID_ARG;
-  if (t->max_depth < 0 || t->max_depth > MEDUSA_MAX_DEPTH) return MEDUSA_ERR_INVALID_ARG;
-  if (!(temperature >= 0.f) || !(eps >= 0.f) || !(delta >= 0.f)) return MEDUSA_ERR_INVALID_ARG;
-  const int N = t->n_nodes;
-  if (!ws || ws_bytes < medusa_typical_accept_workspace_size(B, N)) return MEDUSA_ERR_WORKSPACE;
-  WsCarver wc(ws);
-  int32_t* pass = wc.take<int32_t>((size_t)B * N);
-  int32_t* amax = wc.take<int32_t>((size_t)B * N);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  node_stats_kernel<<<dim3(N, B), kStatThreads, 0, s>>>(logits, tokens, t->parent, N, V, temperature,
-                                                        eps, delta, pass, amax, p_tok_or_null,
-                                                        thr_or_null, d_status);
-  const int threads = (N + 31) / 32 * 32;
-  select_path_kernel<<<B, threads, 0, s>>>(t->parent, t->depth, N, t->max_depth, pass, amax,
-                                           accept_len, path_nodes, next_tok, d_status);
-  return launch_status();
+  medusa_status st = typical_accept_check(logits, tokens, t, B, V, temperature, eps, delta, accept_len, path_nodes,
+                                          next_tok);
+  if (st != MEDUSA_OK) return st;
+  if (!ws || ws_bytes < medusa_typical_accept_workspace_size(B, t->n_nodes, V)) return MEDUSA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return MEDUSA_ERR_INVALID_ARG;
+  return typical_accept_launch(logits, tokens, t, B, V, temperature, eps, delta, accept_len, path_nodes, next_tok,
+                               p_tok_or_null, thr_or_null, static_cast<float4*>(ws), d_status,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
+

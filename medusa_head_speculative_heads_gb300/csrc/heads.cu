@@ -10,10 +10,13 @@
 // used B times.  Two GEMV kernels stream W1 (then fuse SiLU + residual) and W2
 // with 16-byte non-allocating loads, several rows per warp so that each lane
 // keeps 8 independent 16-byte loads in flight, and the vector operand staged in
-// shared memory as fp32.  The top-k runs in two passes: per-chunk candidate
-// lists, then one merge per (row, head).
+// shared memory as fp32.  The top-k is fused: every W2 CTA ranks its own slice
+// of the vocabulary (one warp per batch row) and a small merge kernel ranks
+// the per-CTA candidates of every (row, head).
 #include <float.h>
 #include <limits.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "host_util.h"
@@ -90,16 +93,51 @@ __device__ __forceinline__ void warp_rows(const TW* __restrict__ W, int C, const
     for (int bb = 0; bb < BB; ++bb) acc[i][bb] = warp_sum(acc[i][bb]);
 }
 
+// Warp-level top-k: ranks the n values v[0..n) (index idx[i], or base + i when
+// idx is null) by (value desc, index asc) and writes the best `topk` to
+// out_v/out_i (lane 0 writes).  Each round every lane scans its strided values
+// for the best one ranked strictly behind the previous round's winner, then a
+// shuffle argmax picks the round's winner: no shared state, no block barrier.
+// v/idx should live in shared memory (every round re-reads them).
+__device__ __forceinline__ void warp_topk(const float* v, const int* idx, int n, int base, int topk,
+                                          float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  float pv = INFINITY;
+  int pi = -1;
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int i = lane; i < n; i += 32) {
+      const float val = v[i];
+      const int id = idx ? idx[i] : base + i;
+      if (ranks_ahead(pv, pi, val, id) && ranks_ahead(val, id, bv, bi)) { bv = val; bi = id; }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ranks_ahead(v2, i2, bv, bi)) { bv = v2; bi = i2; }
+    }
+    if (lane == 0) { out_v[r] = bv; out_i[r] = bi; }
+    pv = bv;
+    pi = bi;
+  }
+}
+
 // kFirst = true : rows are W1 rows; x = h (batch rows b0..b0+BB-1);
-//                 out[b][k][j] = SiLU(acc) + h[b][j]          (u, fp32)
-// kFirst = false: rows are W2 rows; x = u[b][k];
-//                 out[b][k][v] = acc                          (z, fp32)
-// Grid (ctas_per_head, K); block 256; dynamic smem BB * C floats.
+//                 u[b][k][j] = SiLU(acc) + h[b][j]                  (fp32)
+// kFirst = false: rows are W2 rows; x = u[b][k]; z = acc goes to `out` when
+//                 requested, and the CTA ranks its own rows: the top-k of its
+//                 slice of every (b, k) vocabulary row is written to
+//                 cand_{v,i}[(b*K + k) * gridDim.x + blockIdx.x][topk].
+// Grid (ctas_per_head, K); block 256; dynamic smem BB * C floats (+ BB * cap
+// floats holding the CTA's logits for the ranking).
 template <typename TW, int BB, bool kFirst>
 __global__ void __launch_bounds__(kGemvThreads)
 heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const float* __restrict__ u,
-                  int B, int b0, int K, int rows_per_head, int C, float* __restrict__ out) {
-  extern __shared__ float xs[];  // [BB][C]
+                  int B, int b0, int K, int rows_per_head, int C, float* __restrict__ out, int topk,
+                  float* __restrict__ cand_v, int* __restrict__ cand_i) {
+  extern __shared__ float xs[];  // [BB][C], then [BB][cap]
   const int k = blockIdx.y;
   for (int idx = threadIdx.x; idx < BB * C; idx += kGemvThreads) {
     int bb = idx / C, c = idx - bb * C, b = b0 + bb;
@@ -111,6 +149,8 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
 
   // Balanced contiguous row ranges: CTA, then warp.
   const int ctas = gridDim.x;
+  const int cap = (rows_per_head + ctas - 1) / ctas;
+  float* zs = xs + BB * C;
   const int r_lo = (int)((long long)rows_per_head * blockIdx.x / ctas);
   const int r_hi = (int)((long long)rows_per_head * (blockIdx.x + 1) / ctas);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -127,7 +167,8 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
       float hv = load_elem<TW>(h, (size_t)b * C + row);
       out[o] = acc / (1.f + expf(-acc)) + hv;
     } else {
-      out[o] = acc;
+      if (out) out[o] = acc;
+      zs[bb * cap + (row - r_lo)] = acc;
     }
   };
 
@@ -148,146 +189,112 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
     for (int bb = 0; bb < BB; ++bb)
       if (lane == (bb & 31)) emit(r, bb, acc[0][bb]);
   }
+  if constexpr (!kFirst) {
+    __syncthreads();
+    for (int bb = warp; bb < BB; bb += kGemvWarps) {
+      const int b = b0 + bb;
+      if (b >= B) continue;
+      const size_t row = ((size_t)b * K + k) * ctas + blockIdx.x;
+      warp_topk(zs + bb * cap, nullptr, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
+    }
+  }
 }
 
 // ------------------------------------------------------------------- top-k
 
-constexpr int kTopkChunk = 2048;  // values per partial CTA
-constexpr int kTopkMaxChunks = 64;
+constexpr int kTopkThreads = 256;
+constexpr int kTopkChunk = 4096;  // (value, index) pairs one CTA stages and ranks
 
-inline int topk_chunks(int V) {
-  int c = ceil_div(V, kTopkChunk);
-  return c < 1 ? 1 : (c > kTopkMaxChunks ? kTopkMaxChunks : c);
+inline int chunks_for(long long n) {
+  long long c = (n + kTopkChunk - 1) / kTopkChunk;
+  return c < 1 ? 1 : (int)c;
 }
 
-// Inserts (v, i) into the thread's sorted list (column `tid` of s_val/s_idx,
-// KC slots, best first) if it ranks ahead of the last kept entry.
-template <int KC, int NT>
-__device__ __forceinline__ void list_insert(float* s_val, int* s_idx, int tid, float v, int i,
-                                            float& worst_v, int& worst_i) {
-  if (!ranks_ahead(v, i, worst_v, worst_i)) return;
-  int pos = KC - 1;
-  while (pos > 0) {
-    float pv = s_val[(pos - 1) * NT + tid];
-    int pi = s_idx[(pos - 1) * NT + tid];
-    if (!ranks_ahead(v, i, pv, pi)) break;
-    s_val[pos * NT + tid] = pv;
-    s_idx[pos * NT + tid] = pi;
-    --pos;
-  }
-  s_val[pos * NT + tid] = v;
-  s_idx[pos * NT + tid] = i;
-  worst_v = s_val[(KC - 1) * NT + tid];
-  worst_i = s_idx[(KC - 1) * NT + tid];
-}
-
-// One CTA ranks either a slice of a dense row (index = column) or a list of
-// (value, index) candidates (x_idx != NULL).  Grid (chunks, rows); writes
-// topk entries per (row, chunk), best first.  Every thread keeps its own
-// sorted list of KC entries in shared memory; the lists are then merged by
-// topk rounds of a block-wide argmax over the list heads.
-template <int KC, int NT>
-__global__ void __launch_bounds__(NT)
-topk_kernel(const float* __restrict__ x, const int* __restrict__ x_idx, int n_per_row, int chunks,
-            int topk, float* __restrict__ out_val, int* __restrict__ out_idx) {
-  __shared__ float s_val[KC * NT];
-  __shared__ int s_idx[KC * NT];
-  __shared__ float w_val[NT / 32];
-  __shared__ int w_idx[NT / 32], w_own[NT / 32];
-  __shared__ int win_own;
-
-  const int tid = threadIdx.x, row = blockIdx.y, chunk = blockIdx.x;
+// One CTA ranks a slice (<= kTopkChunk pairs) of one row: (value, index)
+// pairs, index = column when x_idx is null.  The slice is staged in shared
+// memory once; every warp ranks a sub-slice with warp_topk, then warp 0 ranks
+// the 8 x topk survivors.  Grid (chunks, rows); out[row][chunk][topk].
+__global__ void __launch_bounds__(kTopkThreads)
+topk_block_kernel(const float* __restrict__ x, const int* __restrict__ x_idx, int n_per_row, int chunks,
+                  int topk, float* __restrict__ out_v, int* __restrict__ out_i) {
+  __shared__ float cv[kTopkChunk];
+  __shared__ int ci[kTopkChunk];
+  __shared__ float sv[kTopkThreads / 32 * MEDUSA_MAX_TOPK];
+  __shared__ int si[kTopkThreads / 32 * MEDUSA_MAX_TOPK];
+  const int row = blockIdx.y, chunk = blockIdx.x, warp = threadIdx.x >> 5;
   const int lo = (int)((long long)n_per_row * chunk / chunks);
   const int hi = (int)((long long)n_per_row * (chunk + 1) / chunks);
-#pragma unroll
-  for (int j = 0; j < KC; ++j) {
-    s_val[j * NT + tid] = -INFINITY;
-    s_idx[j * NT + tid] = INT_MAX;
+  const int n = hi - lo;  // <= kTopkChunk by construction of `chunks`
+  const float* xr = x + (size_t)row * n_per_row + lo;
+  const int* xi = x_idx ? x_idx + (size_t)row * n_per_row + lo : nullptr;
+  for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+    cv[i] = xr[i];
+    ci[i] = xi ? xi[i] : lo + i;
   }
-  float worst_v = -INFINITY;
-  int worst_i = INT_MAX;
-  const float* xr = x + (size_t)row * n_per_row;
-  const int* xi = x_idx ? x_idx + (size_t)row * n_per_row : nullptr;
-  for (int p = lo + tid; p < hi; p += NT) {
-    float v = xr[p];
-    int i = xi ? xi[p] : p;
-    list_insert<KC, NT>(s_val, s_idx, tid, v, i, worst_v, worst_i);
-  }
-
-  int head = 0;
-  const int lane = tid & 31, warp = tid >> 5;
-  float* ov = out_val + ((size_t)row * chunks + chunk) * topk;
-  int* oi = out_idx + ((size_t)row * chunks + chunk) * topk;
-  for (int r = 0; r < topk; ++r) {
-    float v = head < KC ? s_val[head * NT + tid] : -INFINITY;
-    int i = head < KC ? s_idx[head * NT + tid] : INT_MAX;
-    int own = tid;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-      int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-      int own2 = __shfl_xor_sync(0xffffffffu, own, o);
-      if (ranks_ahead(v2, i2, v, i) || (v2 == v && i2 == i && own2 < own)) { v = v2; i = i2; own = own2; }
-    }
-    if (lane == 0) { w_val[warp] = v; w_idx[warp] = i; w_own[warp] = own; }
-    __syncthreads();
-    if (tid == 0) {
-      float bv = w_val[0]; int bi = w_idx[0], bo = w_own[0];
-      for (int w = 1; w < NT / 32; ++w)
-        if (ranks_ahead(w_val[w], w_idx[w], bv, bi)) { bv = w_val[w]; bi = w_idx[w]; bo = w_own[w]; }
-      ov[r] = bv;
-      oi[r] = bi;
-      win_own = bo;
-    }
-    __syncthreads();
-    if (tid == win_own) ++head;
-    __syncthreads();
+  __syncthreads();
+  const int w_lo = (int)((long long)n * warp / (kTopkThreads / 32));
+  const int w_hi = (int)((long long)n * (warp + 1) / (kTopkThreads / 32));
+  warp_topk(cv + w_lo, ci + w_lo, w_hi - w_lo, 0, topk, sv + warp * topk, si + warp * topk);
+  __syncthreads();
+  if (warp == 0) {
+    const size_t o = ((size_t)row * chunks + chunk) * topk;
+    warp_topk(sv, si, (kTopkThreads / 32) * topk, 0, topk, out_v + o, out_i + o);
   }
 }
 
-static medusa_status launch_topk(const float* x, int rows, int V, int topk, float* cand_val, int* cand_idx,
-                                 float* out_val, int* out_idx, cudaStream_t s) {
-  const int chunks = topk_chunks(V);
-  auto run = [&](const float* src, const int* src_idx, int n, int nch, float* dv, int* di) {
-    dim3 grid(nch, rows);
-    if (topk <= 4) topk_kernel<4, 256><<<grid, 256, 0, s>>>(src, src_idx, n, nch, topk, dv, di);
-    else if (topk <= 8) topk_kernel<8, 256><<<grid, 256, 0, s>>>(src, src_idx, n, nch, topk, dv, di);
-    else if (topk <= 16) topk_kernel<16, 256><<<grid, 256, 0, s>>>(src, src_idx, n, nch, topk, dv, di);
-    else topk_kernel<32, 128><<<grid, 128, 0, s>>>(src, src_idx, n, nch, topk, dv, di);
-  };
+// Ranks `rows` rows of n pairs.  More than one chunk per row goes through the
+// candidate buffers (rows x chunks x topk) and one more pass, which the
+// callers size so that it fits a single chunk.
+static medusa_status launch_topk(const float* x, const int* x_idx, int rows, int n, int topk, float* cand_val,
+                                 int* cand_idx, float* out_val, int* out_idx, cudaStream_t s) {
+  const int chunks = chunks_for(n);
   if (chunks == 1) {
-    run(x, nullptr, V, 1, out_val, out_idx);
+    topk_block_kernel<<<dim3(1, rows), kTopkThreads, 0, s>>>(x, x_idx, n, 1, topk, out_val, out_idx);
   } else {
-    run(x, nullptr, V, chunks, cand_val, cand_idx);
-    run(cand_val, cand_idx, chunks * topk, 1, out_val, out_idx);
+    topk_block_kernel<<<dim3(chunks, rows), kTopkThreads, 0, s>>>(x, x_idx, n, chunks, topk, cand_val, cand_idx);
+    topk_block_kernel<<<dim3(1, rows), kTopkThreads, 0, s>>>(cand_val, cand_idx, chunks * topk, 1, topk, out_val,
+                                                              out_idx);
   }
   return launch_status();
 }
 
 static size_t topk_ws_bytes(int rows, int V, int topk) {
   WsCarver w(nullptr);
-  w.take<float>((size_t)rows * topk_chunks(V) * topk);
-  w.take<int>((size_t)rows * topk_chunks(V) * topk);
+  w.take<float>((size_t)rows * chunks_for(V) * topk);
+  w.take<int>((size_t)rows * chunks_for(V) * topk);
   return w.used;
 }
 
 // ------------------------------------------------------------------- GEMV launch
 
+// CTAs per head of the W2 pass never exceed this (bounds the candidate lists:
+// max_ctas_per_head * topk / kTopkChunk <= 32 chunks, whose 32 * topk survivors
+// fit one merge chunk).
+inline int max_ctas_per_head(int V) {
+  int c = ceil_div(V, kRowsPerWarp);
+  return c < 4096 ? c : 4096;
+}
+
 template <typename TW, bool kFirst>
-static void launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int B, int b0, int K,
-                           int rows_per_head, int C, float* out, cudaStream_t s) {
-  const size_t smem = (size_t)BB * C * sizeof(float);
+static int launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int B, int b0, int K,
+                          int rows_per_head, int C, float* out, int topk, float* cand_v, int* cand_i,
+                          cudaStream_t s) {
+  int launched = 0;
   auto go = [&](auto kern) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t xs_bytes = (size_t)BB * C * sizeof(float);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvThreads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvThreads, xs_bytes + (kFirst ? 0 : 2048));
     if (per_sm < 1) per_sm = 1;
-    int total = per_sm * device_sm_count();
-    int per_head = total / K;
+    int per_head = per_sm * device_sm_count() / K;
     if (per_head < 1) per_head = 1;
-    int max_useful = ceil_div(rows_per_head, kRowsPerWarp);
+    const int max_useful = kFirst ? ceil_div(rows_per_head, kRowsPerWarp) : max_ctas_per_head(rows_per_head);
     if (per_head > max_useful) per_head = max_useful;
-    kern<<<dim3(per_head, K), kGemvThreads, smem, s>>>(W, h, u, B, b0, K, rows_per_head, C, out);
+    const int cap = ceil_div(rows_per_head, per_head);
+    const size_t smem = xs_bytes + (kFirst ? 0 : (size_t)BB * cap * sizeof(float));
+    kern<<<dim3(per_head, K), kGemvThreads, smem, s>>>(W, h, u, B, b0, K, rows_per_head, C, out, topk, cand_v,
+                                                       cand_i);
+    launched = per_head;
   };
   switch (BB) {
     case 1: go(heads_gemv_kernel<TW, 1, kFirst>); break;
@@ -295,29 +302,41 @@ static void launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int
     case 4: go(heads_gemv_kernel<TW, 4, kFirst>); break;
     default: go(heads_gemv_kernel<TW, 8, kFirst>); break;
   }
+  return launched;
 }
 
+// Returns the CTAs per head of the W2 pass (candidates per (row, head) / topk).
 template <typename TW>
-static void launch_heads_gemv(const TW* h, const TW* w1, const TW* w2, int B, int H, int V, int K,
-                              float* u, float* z, cudaStream_t s) {
+static int launch_heads_gemv(const TW* h, const TW* w1, const TW* w2, int B, int H, int V, int K, int topk,
+                             float* u, float* z_or_null, float* cand_v, int* cand_i, cudaStream_t s) {
   for (int b0 = 0; b0 < B; b0 += kMaxBatchPerPass) {
     int nb = B - b0 < kMaxBatchPerPass ? B - b0 : kMaxBatchPerPass;
     int BB = nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8;
-    launch_gemv_bb<TW, true>(BB, w1, h, nullptr, B, b0, K, H, H, u, s);
+    launch_gemv_bb<TW, true>(BB, w1, h, nullptr, B, b0, K, H, H, u, 0, nullptr, nullptr, s);
   }
+  int cph = 0;
   for (int b0 = 0; b0 < B; b0 += kMaxBatchPerPass) {
     int nb = B - b0 < kMaxBatchPerPass ? B - b0 : kMaxBatchPerPass;
     int BB = nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8;
-    launch_gemv_bb<TW, false>(BB, w2, nullptr, u, B, b0, K, V, H, z, s);
+    int c = launch_gemv_bb<TW, false>(BB, w2, nullptr, u, B, b0, K, V, H, z_or_null, topk, cand_v, cand_i, s);
+    if (b0 == 0) cph = c;
+    else if (c != cph) return -1;  // the candidate layout must match across passes
   }
+  return cph;
 }
 
-static size_t heads_ws_bytes(int B, int H, int V, int K, int topk, bool need_z) {
+static size_t heads_cand(int B, int V, int K, int topk) { return (size_t)B * K * max_ctas_per_head(V) * topk; }
+static size_t heads_cand2(int B, int V, int K, int topk) {
+  return (size_t)B * K * chunks_for((long long)max_ctas_per_head(V) * topk) * topk;
+}
+
+static size_t heads_ws_bytes(int B, int H, int V, int K, int topk) {
   WsCarver w(nullptr);
   w.take<float>((size_t)B * K * H);
-  if (need_z) w.take<float>((size_t)B * K * V);
-  w.take<float>((size_t)B * K * topk_chunks(V) * topk);
-  w.take<int>((size_t)B * K * topk_chunks(V) * topk);
+  w.take<float>(heads_cand(B, V, K, topk));
+  w.take<int>(heads_cand(B, V, K, topk));
+  w.take<float>(heads_cand2(B, V, K, topk));
+  w.take<int>(heads_cand2(B, V, K, topk));
   return w.used;
 }
 
@@ -327,7 +346,7 @@ using namespace medusa;
 
 extern "C" size_t medusa_heads_workspace_size(int B, int H, int V, int K, int topk) {
   if (B <= 0 || H <= 0 || V <= 0 || K <= 0 || topk <= 0) return 0;
-  return heads_ws_bytes(B, H, V, K, topk, true);
+  return heads_ws_bytes(B, H, V, K, topk);
 }
 
 extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void* w2, int B, int H,
@@ -341,22 +360,27 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
   if (!aligned16(h) || !aligned16(w1) || !aligned16(w2)) return MEDUSA_ERR_INVALID_ARG;
   if (logits_or_null && !aligned16(logits_or_null)) return MEDUSA_ERR_INVALID_ARG;
   const int bb_max = B > 4 ? 8 : B > 2 ? 4 : B > 1 ? 2 : 1;
-  if ((size_t)bb_max * H * sizeof(float) > 220 * 1024) return MEDUSA_ERR_UNSUPPORTED;
-  const bool need_z = logits_or_null == nullptr;
-  if (!ws || ws_bytes < heads_ws_bytes(B, H, V, K, topk, need_z)) return MEDUSA_ERR_WORKSPACE;
+  if ((size_t)bb_max * H * sizeof(float) > 200 * 1024) return MEDUSA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < heads_ws_bytes(B, H, V, K, topk)) return MEDUSA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   WsCarver wc(ws);
   float* u = wc.take<float>((size_t)B * K * H);
-  float* z = need_z ? wc.take<float>((size_t)B * K * V) : logits_or_null;
-  float* cv = wc.take<float>((size_t)B * K * topk_chunks(V) * topk);
-  int* ci = wc.take<int>((size_t)B * K * topk_chunks(V) * topk);
+  float* cv = wc.take<float>(heads_cand(B, V, K, topk));
+  int* ci = wc.take<int>(heads_cand(B, V, K, topk));
+  float* cv2 = wc.take<float>(heads_cand2(B, V, K, topk));
+  int* ci2 = wc.take<int>(heads_cand2(B, V, K, topk));
+  int cph;
   if (dt == MEDUSA_BF16)
-    launch_heads_gemv<uint16_t>((const uint16_t*)h, (const uint16_t*)w1, (const uint16_t*)w2, B, H, V, K, u, z, s);
+    cph = launch_heads_gemv<uint16_t>((const uint16_t*)h, (const uint16_t*)w1, (const uint16_t*)w2, B, H, V, K,
+                                      topk, u, logits_or_null, cv, ci, s);
   else
-    launch_heads_gemv<float>((const float*)h, (const float*)w1, (const float*)w2, B, H, V, K, u, z, s);
+    cph = launch_heads_gemv<float>((const float*)h, (const float*)w1, (const float*)w2, B, H, V, K, topk, u,
+                                   logits_or_null, cv, ci, s);
+  if (cph <= 0) return MEDUSA_ERR_CUDA;
   medusa_status st = launch_status();
   if (st != MEDUSA_OK) return st;
-  return launch_topk(z, B * K, V, topk, cv, ci, topk_logit, topk_idx, s);
+  // Merge the per-CTA candidate lists of every (row, head).
+  return launch_topk(cv, ci, B * K, cph * topk, topk, cv2, ci2, topk_logit, topk_idx, s);
 }
 
 extern "C" size_t medusa_head_topk_workspace_size(int rows, int V, int topk) {
@@ -369,10 +393,11 @@ extern "C" medusa_status medusa_head_topk(const float* logits, int rows, int V, 
                                           size_t ws_bytes, medusa_stream_t stream) {
   if (!logits || !topk_idx || !topk_logit || rows < 1 || V < 1) return MEDUSA_ERR_INVALID_ARG;
   if (topk < 1 || topk > MEDUSA_MAX_TOPK || topk > V) return MEDUSA_ERR_INVALID_ARG;
-  if (topk_chunks(V) > 1 && (!ws || ws_bytes < topk_ws_bytes(rows, V, topk))) return MEDUSA_ERR_WORKSPACE;
+  if ((long long)chunks_for(V) * topk > kTopkChunk) return MEDUSA_ERR_UNSUPPORTED;  // V > 2^17 * 32 / topk
+  if (chunks_for(V) > 1 && (!ws || ws_bytes < topk_ws_bytes(rows, V, topk))) return MEDUSA_ERR_WORKSPACE;
   WsCarver wc(ws);
-  float* cv = wc.take<float>((size_t)rows * topk_chunks(V) * topk);
-  int* ci = wc.take<int>((size_t)rows * topk_chunks(V) * topk);
-  return launch_topk(logits, rows, V, topk, cv, ci, topk_logit, topk_idx,
+  float* cv = wc.take<float>((size_t)rows * chunks_for(V) * topk);
+  int* ci = wc.take<int>((size_t)rows * chunks_for(V) * topk);
+  return launch_topk(logits, nullptr, rows, V, topk, cv, ci, topk_logit, topk_idx,
                      reinterpret_cast<cudaStream_t>(stream));
 }

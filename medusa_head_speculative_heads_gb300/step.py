@@ -42,7 +42,7 @@ class VerifyStep:
         dt = B_.MEDUSA_BF16 if dtype == torch.bfloat16 else B_.MEDUSA_F32
         self.ws_heads = B_._ws(L.medusa_heads_workspace_size(B, H, V, K, topk), device)
         self.ws_attn = B_._ws(L.medusa_tree_attention_workspace_size(nl, B, N, Hq, Hkv, d, Lmax, dt), device)
-        self.ws_acc = B_._ws(L.medusa_typical_accept_workspace_size(B, N), device)
+        self.ws_acc = B_._ws(L.medusa_typical_accept_workspace_size(B, N, V), device)
         # the tensor-core attention path reports a workspace for its split-KV partials
         self.attn_launches = 1 if self.ws_attn is None else 2
 
@@ -75,12 +75,36 @@ class VerifyStep:
         self.accept(logits, stream)
         self.compact(kc, vc, kt, vt, prefix_len, stream)
 
+    def capture(self, h, w1, w2, root_tok, prefix_len, q, kc, vc, kt, vt, logits, pre=None, post=None):
+        """Captures the whole step (optionally preceded by `pre()` and followed
+        by `post()`, e.g. host<->device copies) into a CUDA graph; replaying it
+        re-runs the five calls on the same buffers with one launch."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            # one eager run on the capture stream first (one-time set-up outside capture)
+            if pre:
+                pre()
+            self.run(h, w1, w2, root_tok, prefix_len, q, kc, vc, kt, vt, logits, stream=s)
+            if post:
+                post()
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            if pre:
+                pre()
+            self.run(h, w1, w2, root_tok, prefix_len, q, kc, vc, kt, vt, logits, stream=s)
+            if post:
+                post()
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
     def launches_per_step(self) -> int:
         """Kernels the five calls launch (mirrors the library's dispatch)."""
         B, V = self.dims["B"], self.dims["V"]
         passes = -(-B // 8)
-        chunks = min(64, max(1, -(-V // 2048)))
-        heads = 2 * passes + (1 if chunks == 1 else 2)
+        heads = 2 * passes + 1  # W1 and W2 per pass of <= 8 rows, one top-k merge
         attn = self.attn_launches
         return heads + 1 + attn + 2 + 2
 
