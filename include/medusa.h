@@ -230,6 +230,36 @@ medusa_status medusa_typical_accept(const float* logits, const int32_t* tokens,
                                     float* thr_or_null, void* ws, size_t ws_bytes,
                                     int32_t* d_status, medusa_stream_t stream);
 
+/* Allocation-free variant of medusa_typical_accept (the paper has no
+ * counterpart; this is a property of the library, not of the method).
+ * For callers that cannot allocate device memory where they run the step: a
+ * serving loop whose device memory was handed out at start-up (typically to
+ * the KV cache), a plugin living under a host framework that owns every
+ * allocation, or a latency-critical path that must not enter the CUDA
+ * allocator.  Same arguments, results and device error codes as
+ * medusa_typical_accept, minus the workspace: the per-chunk statistics go to
+ * one static device array of MEDUSA_ACCEPT_NOALLOC_MAX_BYTES that every GPU
+ * loading this library holds until the process exits.
+ *  - Limit: medusa_typical_accept_workspace_size(B, N, V) must not exceed
+ *    MEDUSA_ACCEPT_NOALLOC_MAX_BYTES (1 MiB; e.g. B * N <= 4096 at V = 32000),
+ *    else MEDUSA_ERR_UNSUPPORTED before any launch.
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time runtime query, no allocation); make that first call before any
+ *    stream capture on that device.  MEDUSA_ERR_CUDA if the lookup fails.
+ *  - Every call on a device uses the same array and leaves its contents
+ *    behind; each call writes every entry it reads first, so nothing needs
+ *    clearing.  Calls whose kernels overlap on the GPU (different streams
+ *    without ordering) race on the array: order them.
+ *  - Calls no cudaMalloc / cudaFree or other allocating routine. */
+#define MEDUSA_ACCEPT_NOALLOC_MAX_BYTES (1u << 20)
+medusa_status medusa_typical_accept_noalloc(const float* logits, const int32_t* tokens,
+                                            const medusa_dev_topology* t, int B, int V,
+                                            float temperature, float eps, float delta,
+                                            int32_t* accept_len, int32_t* path_nodes,
+                                            int32_t* next_tok, float* p_tok_or_null,
+                                            float* thr_or_null, int32_t* d_status,
+                                            medusa_stream_t stream);
+
 /* ----------------------------------------------------------- (e) kv_compact
  * Appends the accepted path's keys/values to the cache (guide, "树形验证":
  * verification with past_key_values and use_cache):

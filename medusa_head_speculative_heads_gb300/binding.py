@@ -28,7 +28,7 @@ EXPORTS = (
     "medusa_heads", "medusa_head_topk_workspace_size", "medusa_head_topk", "medusa_tree_build",
     "medusa_tree_attention_workspace_size", "medusa_tree_attention",
     "medusa_typical_accept_workspace_size", "medusa_typical_accept", "medusa_kv_compact",
-    "medusa_status_check", "medusa_status_string", "medusa_version",
+    "medusa_status_check", "medusa_status_string", "medusa_version", "medusa_typical_accept_noalloc",
 )
 
 
@@ -84,6 +84,7 @@ def lib():
             "medusa_tree_attention": (I, [P, P, P, P, P, P, P] + [I] * 7 + [F, I, P, P, Z, P, P]),
             "medusa_typical_accept_workspace_size": (Z, [I, I, I]),
             "medusa_typical_accept": (I, [P, P, P, I, I, F, F, F, P, P, P, P, P, P, Z, P, P]),
+            "medusa_typical_accept_noalloc": (I, [P, P, P, I, I, F, F, F, P, P, P, P, P, P, P]),
             "medusa_kv_compact": (I, [P, P, P, P, P, P, P, P] + [I] * 8 + [P, P]),
             "medusa_status_check": (I, [P, P, P]),
             "medusa_status_string": (ctypes.c_char_p, [I]),
@@ -291,6 +292,34 @@ def medusa_typical_accept(logits, tokens, topo: DevTopology, temperature: float,
         _ptr(logits), _ptr(tokens), ctypes.byref(topo.st), B, V, float(temperature), float(eps), float(delta),
         _ptr(accept_len), _ptr(path_nodes), _ptr(next_tok), _ptr(p_tok), _ptr(thr), _ptr(ws),
         0 if ws is None else ws.numel(), _ptr(d_status), _stream(stream)))
+    return accept_len, path_nodes, next_tok, p_tok, thr
+
+
+def medusa_typical_accept_noalloc(logits, tokens, topo: DevTopology, temperature: float, eps: float, delta: float,
+                                  accept_len=None, path_nodes=None, next_tok=None, p_tok=None, thr=None,
+                                  d_status=None, stream=None, want_probs: bool = False):
+    """medusa_typical_accept without a workspace argument: the library's
+    static device scratch is used instead (see include/medusa.h for the size
+    limit).  Output tensors passed in are written in place; missing ones are
+    created here."""
+    import torch
+    B, N, V = logits.shape
+    dev = logits.device
+    D1 = topo.max_depth + 1
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if path_nodes is None:
+        path_nodes = torch.empty((B, D1), dtype=torch.int32, device=dev)
+    if next_tok is None:
+        next_tok = torch.empty(B, dtype=torch.int32, device=dev)
+    if want_probs and p_tok is None:
+        p_tok = torch.empty((B, N), dtype=torch.float32, device=dev)
+    if want_probs and thr is None:
+        thr = torch.empty((B, N), dtype=torch.float32, device=dev)
+    _check("medusa_typical_accept_noalloc", lib().medusa_typical_accept_noalloc(
+        _ptr(logits), _ptr(tokens), ctypes.byref(topo.st), B, V, float(temperature), float(eps), float(delta),
+        _ptr(accept_len), _ptr(path_nodes), _ptr(next_tok), _ptr(p_tok), _ptr(thr), _ptr(d_status),
+        _stream(stream)))
     return accept_len, path_nodes, next_tok, p_tok, thr
 
 

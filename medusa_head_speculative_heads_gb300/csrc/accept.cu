@@ -20,6 +20,8 @@
 // token.
 #include <limits.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "host_util.h"
 
@@ -297,3 +299,59 @@ extern "C" medusa_status medusa_typical_accept(const float* logits, const int32_
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ allocation-free variant
+//
+// For callers that may not allocate device memory at the point where they run
+// the acceptance step: code inside a region whose memory budget was fixed at
+// start-up (the KV cache took the rest of the GPU), plugins that run under a
+// host framework which owns every allocation, or loops that must never call
+// into the CUDA allocator because it can synchronise the device.  The
+// per-chunk statistics live in one static device array instead of a caller
+// workspace.  The array exists once per GPU that loads this library and stays
+// allocated until the process exits.
+
+namespace medusa {
+
+// 1 MiB of float4 partials: B * N * accept_chunks(V) <= 65536.
+constexpr size_t kNoallocScratchBytes = MEDUSA_ACCEPT_NOALLOC_MAX_BYTES;
+static __device__ __align__(256) float4 g_accept_scratch[kNoallocScratchBytes / sizeof(float4)];
+
+// Device address of g_accept_scratch on each device (host code only sees a
+// host-side stand-in for the symbol; it must not be passed to a kernel).
+static std::mutex g_scratch_mu;
+static float4* g_scratch_ptr[64] = {nullptr};
+
+static medusa_status accept_scratch(float4** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MEDUSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) return MEDUSA_ERR_CUDA;
+    g_scratch_ptr[dev] = static_cast<float4*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return MEDUSA_OK;
+}
+
+}  // namespace medusa
+
+extern "C" medusa_status medusa_typical_accept_noalloc(const float* logits, const int32_t* tokens,
+                                                       const medusa_dev_topology* t, int B, int V,
+                                                       float temperature, float eps, float delta,
+                                                       int32_t* accept_len, int32_t* path_nodes,
+                                                       int32_t* next_tok, float* p_tok_or_null,
+                                                       float* thr_or_null, int32_t* d_status,
+                                                       medusa_stream_t stream) {
+  medusa_status st = typical_accept_check(logits, tokens, t, B, V, temperature, eps, delta, accept_len, path_nodes,
+                                          next_tok);
+  if (st != MEDUSA_OK) return st;
+  if (medusa_typical_accept_workspace_size(B, t->n_nodes, V) > kNoallocScratchBytes) return MEDUSA_ERR_UNSUPPORTED;
+  float4* scratch = nullptr;
+  st = accept_scratch(&scratch);
+  if (st != MEDUSA_OK) return st;
+  // node_partial writes every entry the select kernel reads, so nothing in the
+  // array has to start at zero.
+  return typical_accept_launch(logits, tokens, t, B, V, temperature, eps, delta, accept_len, path_nodes, next_tok,
+                               p_tok_or_null, thr_or_null, scratch, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
