@@ -16,8 +16,9 @@
 // SM sub-partitions' exp units) busy.  Otherwise a tile holds 128 rows of one
 // kv head and 128 keys.
 //
-// Roles (256 threads): warp 0 lane 0 issues TMA (Q once per item, K and V per
-// key tile, two stages); warp 1 allocates TMEM and lane 0 issues the MMAs
+// Roles (256 threads): warp 0 lane 0 issues TMA (Q once per item; K and V of
+// every key tile into a five-slot ring of 32 KB half-tiles, a K slot freed as
+// soon as its S = Q K^T is done, a V slot when its P V is done); warp 1 allocates TMEM and lane 0 issues the MMAs
 // (S = Q K^T into one of two S buffers, O += P V); warps 4-7 (one row per
 // thread) read S from TMEM, apply the prefix-length / ancestor mask, keep the
 // online softmax in the log2 domain (O is rescaled in TMEM only when the row
@@ -38,13 +39,13 @@ using namespace sm100;
 namespace tc {
 
 constexpr int kThreads = 256;
-constexpr int kStages = 2;
+constexpr int kSlots = 5;                               // ring of K or V half-tiles
 constexpr uint32_t kHalf = 16384;                       // 128 rows x 128 bytes
 constexpr uint32_t kBox = 8192;                         // 64 rows x 128 bytes
 constexpr uint32_t kOffQ = 0;                           // 2 d-halves
-constexpr uint32_t kOffStage = 2 * kHalf;               // K (2 halves) + V (2 halves) per stage
-constexpr uint32_t kStageBytes = 4 * kHalf;
-constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // 2 key-halves
+constexpr uint32_t kOffRing = 2 * kHalf;                // slot = K or V of one tile (2 d-halves)
+constexpr uint32_t kSlotBytes = 2 * kHalf;
+constexpr uint32_t kOffP = kOffRing + kSlots * kSlotBytes;  // 2 key-halves
 constexpr uint32_t kOffBar = kOffP + 2 * kHalf;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;                     // S0, S1 (128 each), O (128)
@@ -69,9 +70,13 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, o_done, o_free, drain;
 };
+
+// Half-tile c of the load sequence: K of tile g is c = 2g, V of tile g is 2g + 1.
+__device__ __forceinline__ int slot_of(int c) { return c % kSlots; }
+__device__ __forceinline__ uint32_t use_parity(int c) { return (uint32_t)(c / kSlots) & 1u; }
 
 struct Item {
   int lb, b, h0, mt, L, T, n_pre;
@@ -131,10 +136,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
     }
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
@@ -175,7 +179,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int g = 0, n = 0;
+      int g = 0, n = 0, issued = 0;
       bool alive = true;
       for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
         const Item x = decode(p, it);
@@ -191,37 +195,31 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tma_load_5d(smem + kOffQ + dh * kHalf, &tm_q, &bars->q_full, 64 * dh, 0, x.h0, x.mt * (128 / p.G), x.lb);
           }
         }
-        for (int t = 0; t < x.T; ++t, ++g) {
-          const int st = g % kStages;
-          if (g >= kStages &&
-              !(alive = mbar_wait_bounded(&bars->kv_empty[st], ((g / kStages) - 1) & 1, &s_abort, kWaitNs)))
-            break;
+        for (int t = 0; t < x.T && alive; ++t, ++g) {
           const bool tree = t >= x.n_pre;
           const int j0 = (tree ? t - x.n_pre : t) * p.KT;
-          const CUtensorMap* mk = tree ? &tm_kt : &tm_kc;
-          const CUtensorMap* mv = tree ? &tm_vt : &tm_vc;
-          uint8_t* kb = smem + kOffStage + st * kStageBytes;
-          uint8_t* vb = kb + 2 * kHalf;
-          mbar_expect_tx(&bars->k_full[st], 2 * kHalf);
-          for (int dh = 0; dh < 2; ++dh)
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_4d(kb + dh * kHalf + cb * kBox, mk, &bars->k_full[st], 64 * dh,
-                          PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
-          mbar_expect_tx(&bars->v_full[st], 2 * kHalf);
-          for (int dh = 0; dh < 2; ++dh)
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_4d(vb + dh * kHalf + cb * kBox, mv, &bars->v_full[st], 64 * dh,
-                          PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
+          for (int kv = 0; kv < 2; ++kv) {
+            const int c = 2 * g + kv, sl = slot_of(c);
+            if (c >= kSlots &&
+                !(alive = mbar_wait_bounded(&bars->empty[sl], use_parity(c - kSlots), &s_abort, kWaitNs)))
+              break;
+            const CUtensorMap* mp = kv ? (tree ? &tm_vt : &tm_vc) : (tree ? &tm_kt : &tm_kc);
+            uint8_t* dst = smem + kOffRing + sl * kSlotBytes;
+            mbar_expect_tx(&bars->full[sl], kSlotBytes);
+            for (int dh = 0; dh < 2; ++dh)
+              for (int cb = 0; cb < 2; ++cb)
+                tma_load_4d(dst + dh * kHalf + cb * kBox, mp, &bars->full[sl], 64 * dh,
+                            PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
+            issued = c + 1;
+          }
         }
       }
       if (!alive) {
         // Drain: wait (bounded, regardless of the abort flag) for the last
         // phase issued on every load barrier, so no copy lands after exit.
         if (n > 0) mbar_wait_bounded(&bars->q_full, (n - 1) & 1, nullptr, kDrainNs);
-        for (int k = g - 1; k >= 0 && k >= g - kStages; --k) {
-          mbar_wait_bounded(&bars->k_full[k % kStages], (k / kStages) & 1, nullptr, kDrainNs);
-          mbar_wait_bounded(&bars->v_full[k % kStages], (k / kStages) & 1, nullptr, kDrainNs);
-        }
+        for (int c = issued - 1; c >= 0 && c >= issued - kSlots; --c)
+          mbar_wait_bounded(&bars->full[slot_of(c)], use_parity(c), nullptr, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -239,13 +237,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int g0 = g;
       for (int j = 0; j <= x.T && alive; ++j) {
         if (j < x.T) {
-          const int gj = g0 + j, st = gj % kStages, sb = gj & 1;
-          if (!(alive = warp_wait(&bars->k_full[st], (gj / kStages) & 1, &s_abort))) break;
+          const int gj = g0 + j, ck = 2 * gj, sb = gj & 1;
+          if (!(alive = warp_wait(&bars->full[slot_of(ck)], use_parity(ck), &s_abort))) break;
           if (gj >= 2 && !(alive = warp_wait(&bars->s_free[sb], ((gj >> 1) - 1) & 1, &s_abort))) break;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t qa = smem_u32(smem + kOffQ);
-            const uint32_t ka = smem_u32(smem + kOffStage + st * kStageBytes);
+            const uint32_t ka = smem_u32(smem + kOffRing + slot_of(ck) * kSlotBytes);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -253,16 +251,17 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                        kIdescQK, kk > 0);
             }
             mma_commit(&bars->s_full[sb]);
+            mma_commit(&bars->empty[slot_of(ck)]);
             if (j == x.T - 1) mma_commit(&bars->q_empty);
           }
           __syncwarp();
         }
         if (j >= 1) {
-          const int t = j - 1, gt = g0 + t, st = gt % kStages;
+          const int t = j - 1, gt = g0 + t, cv = 2 * gt + 1;
           if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
           if (!(alive = warp_wait(&bars->p_full, pv & 1, &s_abort))) break;
-          if (!(alive = warp_wait(&bars->v_full[st], (gt / kStages) & 1, &s_abort))) break;
-          uint8_t* vb = smem + kOffStage + st * kStageBytes + 2 * kHalf;
+          if (!(alive = warp_wait(&bars->full[slot_of(cv)], use_parity(cv), &s_abort))) break;
+          uint8_t* vb = smem + kOffRing + slot_of(cv) * kSlotBytes;
           // The last prefix tile may run past prefix_len: zero those V rows
           // (stale cache rows may hold anything, and 0 * NaN is NaN).
           const int j0 = t * p.KT;
@@ -287,7 +286,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                        smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, (kk > 0 || t > 0) ? 1u : 0u);
             }
             mma_commit(&bars->o_done);
-            mma_commit(&bars->kv_empty[st]);
+            mma_commit(&bars->empty[slot_of(cv)]);
           }
           __syncwarp();
           ++pv;
@@ -336,31 +335,53 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
         const bool tree = t >= x.n_pre;
         const int j0 = (tree ? t - x.n_pre : t) * p.KT;
-        uint32_t mw[4] = {0u, 0u, 0u, 0u};
-        if (tree && row_ok) {
+        const float sc = p.scale_log2;
+        // Raw-score maximum over the visible keys (scale > 0 keeps the order).
+        float mx = -INFINITY;
+        if (!tree && j0 + p.KT <= x.L && row_ok) {
+          // a prefix tile entirely inside the prefix: every key is visible
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int word = (j0 >> 5) + w;
-            if (w * 32 < ncol && word < p.W) mw[w] = p.mask[(size_t)node * p.W + word];
+          for (int c = 0; c < ncol; ++c) mx = fmaxf(mx, s[c]);
+        } else {
+          uint32_t mw[4] = {0u, 0u, 0u, 0u};
+          if (tree && row_ok) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int word = (j0 >> 5) + w;
+              if (w * 32 < ncol && word < p.W) mw[w] = p.mask[(size_t)node * p.W + word];
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < ncol; ++c) {
+            const int j = j0 + c;
+            const bool v = row_ok && (tree ? (j < p.N && ((mw[c >> 5] >> (c & 31)) & 1u)) : (j < x.L));
+            s[c] = v ? s[c] : -INFINITY;
+            mx = fmaxf(mx, s[c]);
           }
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < ncol; ++c) {
-          const int j = j0 + c;
-          bool v = row_ok && (tree ? (j < p.N && ((mw[c >> 5] >> (c & 31)) & 1u)) : (j < x.L));
-          s[c] = v ? s[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-        const float m_new = fmaxf(m_used, mx);
+        const float m_new = fmaxf(m_used, mx * sc);  // log2 domain
         const bool need = m_new > m_used + 8.f;
+        const float f = need ? fast_exp2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
+        if (need) m_used = m_new;
+        // Probabilities first (overlaps the previous tile's PV), packed to bf16.
+        // exp2(-inf) = 0 covers the masked keys.
+        float rs = 0.f;
+        uint32_t pk[ncol / 2];
+        const float neg = -m_used;
+#pragma unroll
+        for (int c = 0; c < ncol; c += 2) {
+          const float a = m_used == -INFINITY ? 0.f : fast_exp2(fmaf(s[c], sc, neg));
+          const float b2 = m_used == -INFINITY ? 0.f : fast_exp2(fmaf(s[c + 1], sc, neg));
+          rs += a + b2;
+          pk[c >> 1] = pack_bf16x2(a, b2);
+        }
+        l = l * f + rs;
         if (t > 0) {
           // PV of the previous tile must be done before O is touched or P rewritten.
           if (!(alive = warp_wait(&bars->o_done, pv & 1, &s_abort))) break;
           ++pv;
           tc_fence_after();
           if (__any_sync(0xffffffffu, need)) {
-            const float f = need ? fast_exp2(m_used - m_new) : 1.f;
             float o[32];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
@@ -371,28 +392,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               tmem_st32(lane_addr + kColO + 32 * c4, o);
             }
             tmem_wait_st();
-            l *= f;
           }
         }
-        if (need) m_used = m_new;
-        float rs = 0.f;
         uint8_t* prow = smem + kOffP + m * 128;
 #pragma unroll
         for (int c8 = 0; c8 < ncol / 8; ++c8) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = s[c8 * 8 + 2 * e] == -INFINITY ? 0.f : fast_exp2(s[c8 * 8 + 2 * e] - m_used);
-            const float b2 = s[c8 * 8 + 2 * e + 1] == -INFINITY ? 0.f : fast_exp2(s[c8 * 8 + 2 * e + 1] - m_used);
-            rs += a + b2;
-            pk[e] = pack_bf16x2(a, b2);
-          }
           const int kc = (col0 >> 6) + (c8 >> 3);  // key half (P region)
           const int chunk = c8 & 7;
           *reinterpret_cast<uint4*>(prow + kc * kHalf + ((chunk ^ (m & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
         }
-        l += rs;
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->p_full);
@@ -522,8 +531,11 @@ medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, c
   auto kern = p.packed ? tree_attn_tc_kernel<true> : tree_attn_tc_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  int grid = device_sm_count();
-  if (grid > p.items) grid = p.items;
+  // Equal-cost items: as many rounds as the SM count forces, then spread the
+  // items evenly over just enough CTAs (no ragged last round).
+  const int sms = device_sm_count();
+  const int rounds = (p.items + sms - 1) / sms;
+  const int grid = (p.items + rounds - 1) / rounds;
   kern<<<grid, tc::kThreads, tc::kSmemBytes, s>>>(mq, mkc, mvc, mkt, mvt, p);
   return launch_status();
 }
