@@ -203,11 +203,7 @@ def run_ours(args, c):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
 
     # ---- per-call breakdown (separate eager pass, events between the calls)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
@@ -231,7 +227,7 @@ def run_ours(args, c):
     assert vs.check() == 0
 
     ms_per_step = elapsed_ms / K
-    value = world / (ms_per_step / 1e3)
+    value = job_steps_per_s(ms_per_step, world)
     hbm, tflops, peak_src = _peaks()
     ab = algorithmic_bytes(c, N)
     rooflines = {}
@@ -262,21 +258,40 @@ def run_ours(args, c):
         dist.destroy_process_group()
 
 
+def max_over_ranks(elapsed_ms: float, world: int, device) -> float:
+    """The slowest rank's timed region (every rank gets it)."""
+    if world <= 1:
+        return elapsed_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_steps_per_s(ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step, so the
+    job completes `world` steps per (slowest-rank) step time."""
+    return world / (ms_per_step / 1e3)
+
+
 def _traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)
-        ent = t.get(kernel)
-        if not ent:
-            return None
-        import hashlib
-        src = os.path.join(ROOT, "medusa_head_speculative_heads_gb300", "csrc", ent["source"])
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["source_sha"]:
-            return None
-        return ent["dram_bytes_per_launch"]
+        with open(os.path.join(ROOT, "profiles", "traffic.md")) as f:
+            rows = [ln.strip().strip("|").split("|") for ln in f if ln.startswith("| medusa_")]
+        for r in rows:
+            name, src, sha, nbytes = (x.strip() for x in r[:4])
+            if name != kernel:
+                continue
+            path = os.path.join(ROOT, "medusa_head_speculative_heads_gb300", "csrc", src)
+            if hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] != sha:
+                return None
+            return int(nbytes)
     except Exception:
         return None
+    return None
 
 
 def _to_dev(a, dev):

@@ -12,7 +12,7 @@
 // its slice of the node's fp32 logits once for the max/argmax and once more
 // (from L1/L2) for the tempered sums S_c = sum e^((z-m_c)/T) and
 // E_c = sum e^((z-m_c)/T) (z-m_c)/T.  select_path: one CTA per row combines the
-// chunk partials exactly (S = sum_c S_c e^((m_c-m)/T), E likewise), giving
+// chunk partials exactly (a few threads per node and a shuffle reduction) (S = sum_c S_c e^((m_c-m)/T), E likewise), giving
 // H = ln S - E/S and the threshold per node, tests every child against its
 // parent's distribution, propagates acceptance level by level (a node is
 // accepted iff its parent is and it passed), picks the deepest accepted node
@@ -131,58 +131,88 @@ node_partial_kernel(const float* __restrict__ logits, int N, int V, int C, float
   if (tid == 0) part[((size_t)b * N + n) * C + c] = make_float4(mv, __int_as_float(mi), S, E);
 }
 
-// Grid B; block = N rounded up to a warp multiple (<= 256).
-__global__ void __launch_bounds__(MEDUSA_MAX_NODES)
+// Combines two partial statistics (max, argmax, S, E) of one logit row.
+__device__ __forceinline__ void combine_stats(float& m, int& a, float& S, float& E, float m2, int a2, float S2,
+                                              float E2, float inv_t) {
+  float mn = m;
+  int an = a;
+  if (ranks_ahead(m2, a2, m, a)) { mn = m2; an = a2; }
+  float Sn = 0.f, En = 0.f;
+  if (S > 0.f) {
+    const float d = (m - mn) * inv_t, w = expf(d);
+    Sn = S * w;
+    En = w * fmaf(S, d, E);
+  }
+  if (S2 > 0.f) {
+    const float d = (m2 - mn) * inv_t, w = expf(d);
+    Sn = fmaf(S2, w, Sn);
+    En = fmaf(w, fmaf(S2, d, E2), En);
+  }
+  m = mn;
+  a = an;
+  S = Sn;
+  E = En;
+}
+
+constexpr int kSelectThreads = 256;
+
+// Grid B; block 256.  `grp` threads (a power of two <= 8 with grp * N <= 256)
+// combine the chunk partials of one node, then one thread per node tests it
+// against its parent and the tree is resolved level by level.
+__global__ void __launch_bounds__(kSelectThreads)
 select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__ tokens,
                    const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int N, int V,
-                   int max_depth, int C, float T, float eps, float delta, const float4* __restrict__ part,
+                   int max_depth, int C, int grp, float T, float eps, float delta, const float4* __restrict__ part,
                    int32_t* __restrict__ accept_len, int32_t* __restrict__ path_nodes,
                    int32_t* __restrict__ next_tok, float* __restrict__ p_tok, float* __restrict__ thr_out,
                    int32_t* d_status) {
   __shared__ int acc[MEDUSA_MAX_NODES], pass[MEDUSA_MAX_NODES], amax[MEDUSA_MAX_NODES];
   __shared__ float zmax[MEDUSA_MAX_NODES], ssum[MEDUSA_MAX_NODES], thr[MEDUSA_MAX_NODES];
-  __shared__ int s_key[MEDUSA_MAX_NODES / 32];
+  __shared__ int s_key[kSelectThreads / 32];
   __shared__ int s_bad;
-  const int b = blockIdx.x, c = threadIdx.x;
-  if (c == 0) s_bad = 0;
+  const int b = blockIdx.x, tid = threadIdx.x, c = tid;
+  if (tid == 0) s_bad = 0;
+  // 1. statistics of every node: grp threads per node, strided over the chunks
+  {
+    const int node = tid / grp, sub = tid % grp;
+    const float inv_t = T > 0.f ? 1.f / T : 0.f;
+    float m = -INFINITY, S = 0.f, E = 0.f;
+    int a = INT_MAX;
+    if (node < N) {
+      const float4* pp = part + ((size_t)b * N + node) * C;
+      for (int k = sub; k < C; k += grp) {
+        const float4 q = pp[k];
+        combine_stats(m, a, S, E, q.x, __float_as_int(q.y), q.z, q.w, inv_t);
+      }
+    }
+    for (int o = 1; o < grp; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+      const float E2 = __shfl_xor_sync(0xffffffffu, E, o);
+      combine_stats(m, a, S, E, m2, a2, S2, E2, inv_t);
+    }
+    if (node < N && sub == 0) {
+      float th;
+      if (T > 0.f) {
+        const float H = logf(S) - E / S;
+        th = fminf(eps, delta * expf(-H));
+      } else {
+        th = fminf(eps, delta);
+        S = 1.f;
+      }
+      zmax[node] = m;
+      ssum[node] = S;
+      thr[node] = th;
+      amax[node] = a;
+    }
+  }
   __syncthreads();
   int dc = -1, pc = -1;
   if (c < N) {
     dc = depth[c];
     pc = parent[c];
     if (c > 0 && (pc < 0 || pc >= c || dc < 1 || dc > max_depth)) s_bad = 1;
-    // Combine this node's chunk partials.
-    const float4* pp = part + ((size_t)b * N + c) * C;
-    float m = -INFINITY;
-    int a = INT_MAX;
-    for (int k = 0; k < C; ++k) {
-      const float4 q = pp[k];
-      const int qi = __float_as_int(q.y);
-      if (ranks_ahead(q.x, qi, m, a)) { m = q.x; a = qi; }
-    }
-    float th;
-    float S = 1.f;
-    if (T > 0.f) {
-      const float inv_t = 1.f / T;
-      float e = 0.f;
-      S = 0.f;
-      for (int k = 0; k < C; ++k) {
-        const float4 q = pp[k];
-        if (q.z == 0.f) continue;  // an empty chunk
-        const float d = (q.x - m) * inv_t;
-        const float w = expf(d);
-        S = fmaf(q.z, w, S);
-        e = fmaf(w, fmaf(q.z, d, q.w), e);
-      }
-      const float H = logf(S) - e / S;
-      th = fminf(eps, delta * expf(-H));
-    } else {
-      th = fminf(eps, delta);
-    }
-    zmax[c] = m;
-    ssum[c] = S;
-    thr[c] = th;
-    amax[c] = a;
     acc[c] = c == 0 ? 1 : 0;
   }
   __syncthreads();
@@ -266,10 +296,11 @@ medusa_status typical_accept_launch(const float* logits, const int32_t* tokens, 
   const int N = t->n_nodes;
   const int C = accept_chunks(V);
   node_partial_kernel<<<dim3(C, N, B), kPartThreads, 0, s>>>(logits, N, V, C, temperature, part);
-  const int threads = (N + 31) / 32 * 32;
-  select_path_kernel<<<B, threads, 0, s>>>(logits, tokens, t->parent, t->depth, N, V, t->max_depth, C, temperature,
-                                           eps, delta, part, accept_len, path_nodes, next_tok, p_tok_or_null,
-                                           thr_or_null, d_status);
+  int grp = 1;
+  while (grp < 8 && grp * 2 * N <= kSelectThreads) grp *= 2;
+  select_path_kernel<<<B, kSelectThreads, 0, s>>>(logits, tokens, t->parent, t->depth, N, V, t->max_depth, C, grp,
+                                                  temperature, eps, delta, part, accept_len, path_nodes, next_tok,
+                                                  p_tok_or_null, thr_or_null, d_status);
   return launch_status();
 }
 

@@ -7,9 +7,10 @@
 // Paper review, FAQ "树注意力为什么能一次验证多条候选": each token attends only
 // to its own branch's predecessors, and positions follow the tree.
 //
-// One CTA per batch row, one thread per node.  CTA 0 also writes the mask
-// (batch-independent): each thread walks its own ancestor chain (at most
-// MEDUSA_MAX_DEPTH steps) and writes its mask row of ceil(N/32) words.
+// One CTA per batch row, one thread per node; the topology is staged in
+// shared memory first.  CTA 0 also writes the mask (batch-independent): each
+// thread walks its own ancestor chain (at most MEDUSA_MAX_DEPTH steps) and
+// writes its mask row of ceil(N/32) words.
 #include "common.cuh"
 #include "host_util.h"
 
@@ -23,9 +24,15 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
                   const int32_t* __restrict__ topk_idx, int K, int topk,
                   const int32_t* __restrict__ prefix_len, int32_t* __restrict__ tokens,
                   int32_t* __restrict__ pos, uint32_t* __restrict__ mask, int32_t* d_status) {
+  __shared__ int s_parent[MEDUSA_MAX_NODES], s_depth[MEDUSA_MAX_NODES];
   const int b = blockIdx.x, n = threadIdx.x;
+  if (n < N) {
+    s_parent[n] = parent[n];
+    s_depth[n] = depth[n];
+  }
+  __syncthreads();
   if (n >= N) return;
-  const int dn = depth[n];
+  const int dn = s_depth[n];
   int tok;
   if (n == 0) {
     tok = root_tok[b];
@@ -53,8 +60,8 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
 #pragma unroll
       for (int w = 0; w < kMaskWords; ++w)
         if (w == (a >> 5)) row[w] |= 1u << (a & 31);
-      const int p = parent[a];
-      if (a > 0 && (p >= a || p < 0 || depth[p] != depth[a] - 1)) { ok = false; break; }
+      const int p = s_parent[a];
+      if (a > 0 && (p >= a || p < 0 || s_depth[p] != s_depth[a] - 1)) { ok = false; break; }
       a = a == 0 ? -1 : p;
       ++steps;
     }
