@@ -11,8 +11,9 @@
 // with 16-byte non-allocating loads, several rows per warp so that each lane
 // keeps 8 independent 16-byte loads in flight, and the vector operand staged in
 // shared memory as fp32.  The top-k is fused: every W2 CTA ranks its own slice
-// of the vocabulary (one warp per batch row) and a small merge kernel ranks
-// the per-CTA candidates of every (row, head).
+// of the vocabulary (one warp per batch row) and the last CTA of each head
+// merges the per-CTA candidate lists (a separate merge kernel only when they
+// do not fit its shared memory).
 #include <float.h>
 #include <limits.h>
 
@@ -124,6 +125,42 @@ __device__ __forceinline__ void warp_topk(const float* v, const int* idx, int n,
   }
 }
 
+// Warp-level merge of `nlists` lists, each sorted best first and `len` long
+// (v/idx[list * len + j]), into the best `topk` (lane 0 writes out_v/out_i).
+// Each round compares only the lists' current heads; hp[] (shared memory,
+// nlists ints) holds the head positions.
+__device__ __forceinline__ void warp_merge_sorted(const float* v, const int* idx, int nlists, int len, int topk,
+                                                  int* hp, float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  for (int L = lane; L < nlists; L += 32) hp[L] = 0;
+  __syncwarp();
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX, bl = -1;
+    for (int L = lane; L < nlists; L += 32) {
+      const int hpos = hp[L];
+      if (hpos < len) {
+        const float val = v[L * len + hpos];
+        const int id = idx[L * len + hpos];
+        if (ranks_ahead(val, id, bv, bi)) { bv = val; bi = id; bl = L; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int l2 = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (ranks_ahead(v2, i2, bv, bi)) { bv = v2; bi = i2; bl = l2; }
+    }
+    if (lane == 0) {
+      out_v[r] = bv;
+      out_i[r] = bi;
+      if (bl >= 0) hp[bl] += 1;
+    }
+    __syncwarp();
+  }
+}
+
 // kFirst = true : rows are W1 rows; x = h (batch rows b0..b0+BB-1);
 //                 u[b][k][j] = SiLU(acc) + h[b][j]                  (fp32)
 // kFirst = false: rows are W2 rows; x = u[b][k]; z = acc goes to `out` when
@@ -136,9 +173,16 @@ template <typename TW, int BB, bool kFirst>
 __global__ void __launch_bounds__(kGemvThreads)
 heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const float* __restrict__ u,
                   int B, int b0, int K, int rows_per_head, int C, float* __restrict__ out, int topk,
-                  float* __restrict__ cand_v, int* __restrict__ cand_i) {
+                  float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters,
+                  int n_counters, float* __restrict__ top_v, int* __restrict__ top_i) {
   extern __shared__ float xs[];  // [BB][C], then [BB][cap]
+  __shared__ int s_last;
   const int k = blockIdx.y;
+  if constexpr (kFirst) {
+    // The W2 passes that follow count their finished CTAs here.
+    if (b0 == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      for (int i = threadIdx.x; i < n_counters; i += kGemvThreads) counters[i] = 0;
+  }
   for (int idx = threadIdx.x; idx < BB * C; idx += kGemvThreads) {
     int bb = idx / C, c = idx - bb * C, b = b0 + bb;
     float v = 0.f;
@@ -196,6 +240,40 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
       if (b >= B) continue;
       const size_t row = ((size_t)b * K + k) * ctas + blockIdx.x;
       warp_topk(zs + bb * cap, nullptr, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
+    }
+    if (top_v) {
+      // The last CTA of this head (in this batch pass) merges every CTA's
+      // sorted candidate list: candidates are published with a fence before
+      // the counter increment, and read back through L2.
+      __threadfence();
+      __syncthreads();
+      int* cnt = counters + (b0 / kMaxBatchPerPass) * K + k;
+      if (threadIdx.x == 0) s_last = atomicAdd(cnt, 1) == ctas - 1;
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        float* mv = xs;  // the staged x is no longer needed: [BB][ctas * topk] values
+        int* mi = reinterpret_cast<int*>(xs + BB * ctas * topk);
+        int* hp = mi + BB * ctas * topk;
+        for (int bb = 0; bb < BB; ++bb) {
+          const int b = b0 + bb;
+          if (b >= B) continue;
+          const size_t base = ((size_t)b * K + k) * ctas * topk;
+          for (int i = threadIdx.x; i < ctas * topk; i += kGemvThreads) {
+            mv[bb * ctas * topk + i] = __ldcg(cand_v + base + i);
+            mi[bb * ctas * topk + i] = __ldcg(cand_i + base + i);
+          }
+        }
+        __syncthreads();
+        for (int bb = warp; bb < BB; bb += kGemvWarps) {
+          const int b = b0 + bb;
+          if (b >= B) continue;
+          const size_t o = ((size_t)b * K + k) * topk;
+          warp_merge_sorted(mv + bb * ctas * topk, mi + bb * ctas * topk, ctas, topk, topk, hp + warp * ctas,
+                            top_v + o, top_i + o);
+        }
+        if (threadIdx.x == 0) *cnt = 0;
+      }
     }
   }
 }
@@ -275,16 +353,22 @@ inline int max_ctas_per_head(int V) {
   return c < 4096 ? c : 4096;
 }
 
+// The merge fits the W2 CTA's shared memory (staged x region) when every
+// batch row's ctas * topk (value, index) pairs plus one head position per list
+// fit in C floats.
+inline bool merge_fits(int ctas, int topk, int C) { return (size_t)ctas * topk * 2 + ctas <= (size_t)C; }
+
 template <typename TW, bool kFirst>
 static int launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int B, int b0, int K,
                           int rows_per_head, int C, float* out, int topk, float* cand_v, int* cand_i,
-                          cudaStream_t s) {
+                          int* counters, int n_counters, float* top_v, int* top_i, cudaStream_t s) {
   int launched = 0;
   auto go = [&](auto kern) {
     const size_t xs_bytes = (size_t)BB * C * sizeof(float);
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    const size_t est = xs_bytes + (kFirst ? 0 : 2048);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)est);
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvThreads, xs_bytes + (kFirst ? 0 : 2048));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvThreads, est);
     if (per_sm < 1) per_sm = 1;
     int per_head = per_sm * device_sm_count() / K;
     if (per_head < 1) per_head = 1;
@@ -292,8 +376,11 @@ static int launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int 
     if (per_head > max_useful) per_head = max_useful;
     const int cap = ceil_div(rows_per_head, per_head);
     const size_t smem = xs_bytes + (kFirst ? 0 : (size_t)BB * cap * sizeof(float));
+    if (smem > est) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const bool fuse = !kFirst && top_v && merge_fits(per_head, topk, C);
     kern<<<dim3(per_head, K), kGemvThreads, smem, s>>>(W, h, u, B, b0, K, rows_per_head, C, out, topk, cand_v,
-                                                       cand_i);
+                                                       cand_i, counters, n_counters, fuse ? top_v : nullptr,
+                                                       fuse ? top_i : nullptr);
     launched = per_head;
   };
   switch (BB) {
@@ -308,17 +395,21 @@ static int launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int 
 // Returns the CTAs per head of the W2 pass (candidates per (row, head) / topk).
 template <typename TW>
 static int launch_heads_gemv(const TW* h, const TW* w1, const TW* w2, int B, int H, int V, int K, int topk,
-                             float* u, float* z_or_null, float* cand_v, int* cand_i, cudaStream_t s) {
+                             float* u, float* z_or_null, float* cand_v, int* cand_i, int* counters,
+                             float* top_v, int* top_i, cudaStream_t s) {
+  const int n_counters = ceil_div(B, kMaxBatchPerPass) * K;
   for (int b0 = 0; b0 < B; b0 += kMaxBatchPerPass) {
     int nb = B - b0 < kMaxBatchPerPass ? B - b0 : kMaxBatchPerPass;
     int BB = nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8;
-    launch_gemv_bb<TW, true>(BB, w1, h, nullptr, B, b0, K, H, H, u, 0, nullptr, nullptr, s);
+    launch_gemv_bb<TW, true>(BB, w1, h, nullptr, B, b0, K, H, H, u, 0, nullptr, nullptr, counters, n_counters,
+                             nullptr, nullptr, s);
   }
   int cph = 0;
   for (int b0 = 0; b0 < B; b0 += kMaxBatchPerPass) {
     int nb = B - b0 < kMaxBatchPerPass ? B - b0 : kMaxBatchPerPass;
     int BB = nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8;
-    int c = launch_gemv_bb<TW, false>(BB, w2, nullptr, u, B, b0, K, V, H, z_or_null, topk, cand_v, cand_i, s);
+    int c = launch_gemv_bb<TW, false>(BB, w2, nullptr, u, B, b0, K, V, H, z_or_null, topk, cand_v, cand_i,
+                                      counters, n_counters, top_v, top_i, s);
     if (b0 == 0) cph = c;
     else if (c != cph) return -1;  // the candidate layout must match across passes
   }
@@ -337,6 +428,7 @@ static size_t heads_ws_bytes(int B, int H, int V, int K, int topk) {
   w.take<int>(heads_cand(B, V, K, topk));
   w.take<float>(heads_cand2(B, V, K, topk));
   w.take<int>(heads_cand2(B, V, K, topk));
+  w.take<int>((size_t)ceil_div(B, kMaxBatchPerPass) * K);
   return w.used;
 }
 
@@ -369,17 +461,19 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
   int* ci = wc.take<int>(heads_cand(B, V, K, topk));
   float* cv2 = wc.take<float>(heads_cand2(B, V, K, topk));
   int* ci2 = wc.take<int>(heads_cand2(B, V, K, topk));
+  int* counters = wc.take<int>((size_t)ceil_div(B, kMaxBatchPerPass) * K);
   int cph;
   if (dt == MEDUSA_BF16)
     cph = launch_heads_gemv<uint16_t>((const uint16_t*)h, (const uint16_t*)w1, (const uint16_t*)w2, B, H, V, K,
-                                      topk, u, logits_or_null, cv, ci, s);
+                                      topk, u, logits_or_null, cv, ci, counters, topk_logit, topk_idx, s);
   else
     cph = launch_heads_gemv<float>((const float*)h, (const float*)w1, (const float*)w2, B, H, V, K, topk, u,
-                                   logits_or_null, cv, ci, s);
+                                   logits_or_null, cv, ci, counters, topk_logit, topk_idx, s);
   if (cph <= 0) return MEDUSA_ERR_CUDA;
   medusa_status st = launch_status();
   if (st != MEDUSA_OK) return st;
-  // Merge the per-CTA candidate lists of every (row, head).
+  if (merge_fits(cph, topk, H)) return MEDUSA_OK;  // the W2 pass merged the candidates itself
+  // Otherwise merge the per-CTA candidate lists of every (row, head) here.
   return launch_topk(cv, ci, B * K, cph * topk, topk, cv2, ci2, topk_logit, topk_idx, s);
 }
 
