@@ -421,7 +421,35 @@ static size_t heads_cand2(int B, int V, int K, int topk) {
   return (size_t)B * K * chunks_for((long long)max_ctas_per_head(V) * topk) * topk;
 }
 
+// tensor-core path (heads_tc.cu)
+int heads_tc_bp(int B);
+bool heads_tc_supported(int B, int H, const void* h, const void* w1, const void* w2);
+medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t* w2, int B, int H, int V, int K,
+                           uint16_t* u2, float* z, int32_t* d_status, cudaStream_t s);
+
+// Scratch of the tensor-core path: u split into hi/lo bf16 rows, z, top-k candidates.
+static size_t heads_tc_ws_bytes(int B, int H, int V, int K, int topk) {
+  WsCarver w(nullptr);
+  w.take<uint16_t>((size_t)K * 2 * heads_tc_bp(B) * H);
+  w.take<float>((size_t)B * K * V);
+  w.take<float>((size_t)B * K * chunks_for(V) * topk);
+  w.take<int>((size_t)B * K * chunks_for(V) * topk);
+  return w.used;
+}
+
 static size_t heads_ws_bytes(int B, int H, int V, int K, int topk) {
+  if (B >= 8 && B <= 64 && H % 64 == 0) {
+    // either path may run (the tensor-core one for bf16): size for both
+    const size_t a = heads_tc_ws_bytes(B, H, V, K, topk);
+    WsCarver w(nullptr);
+    w.take<float>((size_t)B * K * H);
+    w.take<float>(heads_cand(B, V, K, topk));
+    w.take<int>(heads_cand(B, V, K, topk));
+    w.take<float>(heads_cand2(B, V, K, topk));
+    w.take<int>(heads_cand2(B, V, K, topk));
+    w.take<int>((size_t)ceil_div(B, kMaxBatchPerPass) * K);
+    return a > w.used ? a : w.used;
+  }
   WsCarver w(nullptr);
   w.take<float>((size_t)B * K * H);
   w.take<float>(heads_cand(B, V, K, topk));
@@ -445,7 +473,6 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
                                       int V, int K, int topk, medusa_dtype dt, int32_t* topk_idx,
                                       float* topk_logit, float* logits_or_null, void* ws,
                                       size_t ws_bytes, int32_t* d_status, medusa_stream_t stream) {
-  (void)d_status;
   if (!h || !w1 || !w2 || !topk_idx || !topk_logit) return MEDUSA_ERR_INVALID_ARG;
   if (B < 1 || B > 64 || H < 8 || H % 8 || V < 1 || K < 1 || K > MEDUSA_MAX_DEPTH) return MEDUSA_ERR_INVALID_ARG;
   if (topk < 1 || topk > MEDUSA_MAX_TOPK || topk > V || !dtype_ok(dt)) return MEDUSA_ERR_INVALID_ARG;
@@ -455,6 +482,19 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
   if ((size_t)bb_max * H * sizeof(float) > 200 * 1024) return MEDUSA_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < heads_ws_bytes(B, H, V, K, topk)) return MEDUSA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == MEDUSA_BF16 && heads_tc_supported(B, H, h, w1, w2)) {
+    // Batches of 8 and more: both passes on tensor cores, then the top-k of z.
+    WsCarver wt(ws);
+    uint16_t* u2 = wt.take<uint16_t>((size_t)K * 2 * heads_tc_bp(B) * H);
+    float* zt = wt.take<float>((size_t)B * K * V);
+    float* cvt = wt.take<float>((size_t)B * K * chunks_for(V) * topk);
+    int* cit = wt.take<int>((size_t)B * K * chunks_for(V) * topk);
+    float* z = logits_or_null ? logits_or_null : zt;
+    medusa_status st = heads_tc_run((const uint16_t*)h, (const uint16_t*)w1, (const uint16_t*)w2, B, H, V, K, u2, z,
+                                    d_status, s);
+    if (st != MEDUSA_OK) return st;
+    return launch_topk(z, nullptr, B * K, V, topk, cvt, cit, topk_logit, topk_idx, s);
+  }
   WsCarver wc(ws);
   float* u = wc.take<float>((size_t)B * K * H);
   float* cv = wc.take<float>(heads_cand(B, V, K, topk));

@@ -1,0 +1,278 @@
+// Medusa heads at decode batches of 8 and more, on tcgen05 tensor cores.
+//
+// Paper review ("Medusa: Simple LLM Inference Acceleration Framework with
+// Multiple Decoding Heads"), section "Medusa 的三个核心组件":
+// p^(k) = softmax(W2^(k) (SiLU(W1^(k) h) + h)).  At B >= 8 the weight stream is
+// a real (skinny) matrix product, so both passes run as
+//   D[128 weight rows, N] = W_tile[128, H] x X^T[H, N]
+// with bf16 operands and an fp32 accumulator in tensor memory.  X holds the
+// batch rows twice: rows 0..Bp-1 are the bf16 "hi" part of the fp32 vector and
+// rows Bp..2Bp-1 the "lo" remainder (v = hi + lo to ~2^-16), so the epilogue
+// sums D[:, b] + D[:, Bp + b] and the product keeps the fp32 vector's
+// precision.  For W1, X = h (exact in bf16: no lo part; those rows are the
+// TMA's zero fill); the W1 epilogue applies SiLU and the residual and writes u
+// split into hi/lo for W2.  The W2 epilogue writes the fp32 logits z, which
+// the regular top-k kernels then rank.
+//
+// Roles (256 threads, one CTA per SM, persistent over 128-row tiles): warp 0
+// lane 0 issues TMA loads of the A (weights) and B (vector) tiles into a
+// six-stage ring; warp 1 allocates TMEM and lane 0 issues the MMAs (four
+// K=16 steps per 64-column stage) into one of two accumulators; warps 4-7
+// read the accumulator (one row per thread) and write the outputs, so the
+// epilogue of one tile overlaps the main loop of the next.  Every wait is
+// bounded; a timeout sets MEDUSA_DEV_TIMEOUT and the kernel drains its
+// copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "sm100.cuh"
+
+namespace medusa {
+using namespace sm100;
+
+namespace htc {
+
+constexpr int kThreads = 256;
+constexpr int kStages = 6;
+constexpr uint32_t kATile = 16384;  // 128 rows x 128 bytes
+constexpr uint32_t kBTile = 16384;  // up to 128 rows x 128 bytes
+constexpr uint32_t kStageBytes = kATile + kBTile;
+constexpr uint32_t kOffBar = kStages * kStageBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
+
+struct Params {
+  int K, R, H, B, Bp, N;  // R rows per head, N = 2 * Bp
+  int tiles_per_head, tiles;
+  int first;              // 1: W1 pass, 0: W2 pass
+  const uint16_t* h;      // [B][H] bf16 (W1 residual)
+  uint16_t* u2;           // [K][N][H] bf16, W1 output (hi rows, then lo rows)
+  float* z;               // [B][K][R] fp32, W2 output
+  int32_t* d_status;
+};
+
+struct Bars {
+  uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, kWaitNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace htc
+
+__global__ void __launch_bounds__(htc::kThreads, 1)
+heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const htc::Params p) {
+  using namespace htc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->acc_full[s], 1);
+      mbar_init(&bars->acc_empty[s], 128);
+    }
+    mbar_init(&bars->drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tm_a);
+    tma_prefetch(&tm_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int ksteps = p.H / 64;
+  const uint32_t b_bytes = (uint32_t)p.N * 128;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int g = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < p.tiles && alive; tile += gridDim.x) {
+        const int k = tile / p.tiles_per_head, m0 = (tile % p.tiles_per_head) * 128;
+        for (int kk = 0; kk < ksteps; ++kk, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages &&
+              !(alive = mbar_wait_bounded(&bars->empty[s], ((g / kStages) - 1) & 1, &s_abort, kWaitNs)))
+            break;
+          uint8_t* st = smem + s * kStageBytes;
+          mbar_expect_tx(&bars->full[s], kATile + b_bytes);
+          tma_load_2d(st, &tm_a, &bars->full[s], kk * 64, k * p.R + m0);
+          tma_load_2d(st + kATile, &tm_b, &bars->full[s], kk * 64, p.first ? 0 : k * p.N);
+        }
+      }
+      if (!alive)
+        for (int c = g - 1; c >= 0 && c >= g - kStages; --c)
+          mbar_wait_bounded(&bars->full[c % kStages], (c / kStages) & 1, nullptr, kDrainNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, p.N, false, false);
+    int g = 0, tc = 0;
+    bool alive = true;
+    for (int tile = blockIdx.x; tile < p.tiles && alive; tile += gridDim.x, ++tc) {
+      const int ab = tc & 1;
+      if (tc >= 2 && !(alive = warp_wait(&bars->acc_empty[ab], ((tc >> 1) - 1) & 1, &s_abort))) break;
+      tc_fence_after();
+      for (int kk = 0; kk < ksteps; ++kk, ++g) {
+        const int s = g % kStages;
+        if (!(alive = warp_wait(&bars->full[s], (g / kStages) & 1, &s_abort))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a = smem_u32(smem + s * kStageBytes);
+          const uint32_t b = a + kATile;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_bf16(tmem + ab * 128, smem_desc_sw128(a + j * 32, 16, 1024), smem_desc_sw128(b + j * 32, 16, 1024),
+                     idesc, (kk > 0 || j > 0) ? 1u : 0u);
+          mma_commit(&bars->empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!alive) break;
+      if (lane == 0) mma_commit(&bars->acc_full[ab]);
+      __syncwarp();
+    }
+    if (!alive && lane == 0) {
+      mma_commit(&bars->drain);
+      mbar_wait_bounded(&bars->drain, 0, nullptr, kDrainNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int m = threadIdx.x - 128;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
+    int tc = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tc) {
+      const int ab = tc & 1;
+      if (!warp_wait(&bars->acc_full[ab], (tc >> 1) & 1, &s_abort)) break;
+      tc_fence_after();
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c * 32 < p.N) tmem_ld32(lane_addr + ab * 128 + c * 32, v + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty[ab]);
+      const int k = tile / p.tiles_per_head, row = (tile % p.tiles_per_head) * 128 + m;
+      if (row >= p.R) continue;
+#pragma unroll
+      for (int b = 0; b < 64; ++b) {
+        if (b >= p.Bp) break;
+        const float zsum = v[b] + v[p.Bp + b];
+        if (p.first) {
+          float val = 0.f;
+          if (b < p.B) val = zsum / (1.f + expf(-zsum)) + bf16_bits_to_f32(p.h[(size_t)b * p.H + row]);
+          const uint32_t hi = f32_to_bf16_bits(val);
+          const uint32_t lo = f32_to_bf16_bits(val - bf16_bits_to_f32(hi));
+          p.u2[((size_t)k * p.N + b) * p.H + row] = (uint16_t)hi;
+          p.u2[((size_t)k * p.N + p.Bp + b) * p.H + row] = (uint16_t)lo;
+        } else if (b < p.B) {
+          p.z[((size_t)b * p.K + k) * p.R + row] = zsum;
+        }
+      }
+    }
+  }
+
+  if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 heads_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 map over rows of H elements: box 64 columns x box_rows rows, 128-byte swizzle.
+static bool map_rows(CUtensorMap* m, const void* base, int H, long long rows, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return heads_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Padded batch of the tensor-core heads path (N = 2 * Bp columns, a multiple of 32).
+int heads_tc_bp(int B) { return (B + 15) / 16 * 16; }
+
+bool heads_tc_supported(int B, int H, const void* h, const void* w1, const void* w2) {
+  return B >= 8 && B <= 64 && H % 64 == 0 && H >= 64 && aligned16(h) && aligned16(w1) && aligned16(w2) &&
+         heads_encode_fn() != nullptr;
+}
+
+// Both passes: u2 = split(SiLU(W1 h) + h) ([K][2Bp][H] bf16, caller scratch),
+// then z = W2 u ([B][K][V] fp32).
+medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t* w2, int B, int H, int V, int K,
+                           uint16_t* u2, float* z, int32_t* d_status, cudaStream_t s) {
+  const int Bp = heads_tc_bp(B), N = 2 * Bp;
+  CUtensorMap ma1, mb1, ma2, mb2;
+  if (!map_rows(&ma1, w1, H, (long long)K * H, 128) || !map_rows(&mb1, h, H, B, N) ||
+      !map_rows(&ma2, w2, H, (long long)K * V, 128) || !map_rows(&mb2, u2, H, (long long)K * N, N))
+    return MEDUSA_ERR_CUDA;
+  if (cudaFuncSetAttribute(heads_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)htc::kSmemBytes) !=
+      cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  const int sms = device_sm_count();
+  htc::Params p{};
+  p.K = K;
+  p.H = H;
+  p.B = B;
+  p.Bp = Bp;
+  p.N = N;
+  p.h = h;
+  p.u2 = u2;
+  p.z = z;
+  p.d_status = d_status;
+  // W1: rows per head = H
+  p.R = H;
+  p.first = 1;
+  p.tiles_per_head = ceil_div(H, 128);
+  p.tiles = K * p.tiles_per_head;
+  heads_tc_kernel<<<p.tiles < sms ? p.tiles : sms, htc::kThreads, htc::kSmemBytes, s>>>(ma1, mb1, p);
+  // W2: rows per head = V
+  p.R = V;
+  p.first = 0;
+  p.tiles_per_head = ceil_div(V, 128);
+  p.tiles = K * p.tiles_per_head;
+  heads_tc_kernel<<<p.tiles < sms ? p.tiles : sms, htc::kThreads, htc::kSmemBytes, s>>>(ma2, mb2, p);
+  return launch_status();
+}
+
+}  // namespace medusa
