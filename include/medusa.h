@@ -141,9 +141,11 @@ medusa_status medusa_topology_upload(const medusa_topology* t, int32_t* d_buf, s
  *   topk_logit [B][K][topk]  fp32 out
  *   logits_or_null [B][K][V] fp32 out, optional (all head logits z)
  * 1 <= B <= 64, 1 <= K <= MEDUSA_MAX_DEPTH, 1 <= topk <= min(V, MEDUSA_MAX_TOPK),
- * H a multiple of 8, pointers 16-byte aligned.  The workspace holds u and the
- * per-CTA candidate lists the W2 pass ranks; z is written only to
- * logits_or_null. */
+ * H a multiple of 8, pointers 16-byte aligned.  bf16 batches of 4 to 64 with H
+ * a multiple of 64 run both passes on tcgen05 tensor cores (the fp32 u split
+ * into bf16 hi + lo operands); smaller batches and fp32 stream the weights on
+ * CUDA cores.  The workspace holds u, the logits z when logits_or_null is NULL
+ * and the top-k candidate lists. */
 size_t medusa_heads_workspace_size(int B, int H, int V, int K, int topk);
 medusa_status medusa_heads(const void* h, const void* w1, const void* w2, int B, int H, int V,
                            int K, int topk, medusa_dtype dt, int32_t* topk_idx, float* topk_logit,

@@ -438,7 +438,7 @@ static size_t heads_tc_ws_bytes(int B, int H, int V, int K, int topk) {
 }
 
 static size_t heads_ws_bytes(int B, int H, int V, int K, int topk) {
-  if (B >= 8 && B <= 64 && H % 64 == 0) {
+  if (B >= 4 && B <= 64 && H % 64 == 0) {
     // either path may run (the tensor-core one for bf16): size for both
     const size_t a = heads_tc_ws_bytes(B, H, V, K, topk);
     WsCarver w(nullptr);
@@ -483,7 +483,7 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
   if (!ws || ws_bytes < heads_ws_bytes(B, H, V, K, topk)) return MEDUSA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dt == MEDUSA_BF16 && heads_tc_supported(B, H, h, w1, w2)) {
-    // Batches of 8 and more: both passes on tensor cores, then the top-k of z.
+    // Batches of 4 and more: both passes on tensor cores, then the top-k of z.
     WsCarver wt(ws);
     uint16_t* u2 = wt.take<uint16_t>((size_t)K * 2 * heads_tc_bp(B) * H);
     float* zt = wt.take<float>((size_t)B * K * V);

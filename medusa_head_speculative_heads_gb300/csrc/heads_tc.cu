@@ -1,8 +1,8 @@
-// Medusa heads at decode batches of 8 and more, on tcgen05 tensor cores.
+// Medusa heads at decode batches of 4 and more, on tcgen05 tensor cores.
 //
 // Paper review ("Medusa: Simple LLM Inference Acceleration Framework with
 // Multiple Decoding Heads"), section "Medusa 的三个核心组件":
-// p^(k) = softmax(W2^(k) (SiLU(W1^(k) h) + h)).  At B >= 8 the weight stream is
+// p^(k) = softmax(W2^(k) (SiLU(W1^(k) h) + h)).  At B >= 4 the weight stream is
 // a real (skinny) matrix product, so both passes run as
 //   D[128 weight rows, N] = W_tile[128, H] x X^T[H, N]
 // with bf16 operands and an fp32 accumulator in tensor memory.  X holds the
@@ -66,9 +66,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 }  // namespace htc
 
+template <int BP>
 __global__ void __launch_bounds__(htc::kThreads, 1)
 heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const htc::Params p) {
+  constexpr int NC = 2 * BP;  // accumulator columns
   using namespace htc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -167,26 +169,24 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       const int ab = tc & 1;
       if (!warp_wait(&bars->acc_full[ab], (tc >> 1) & 1, &s_abort)) break;
       tc_fence_after();
-      float v[128];
+      float v[NC];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c * 32 < p.N) tmem_ld32(lane_addr + ab * 128 + c * 32, v + c * 32);
+      for (int c = 0; c < NC / 32; ++c) tmem_ld32(lane_addr + ab * 128 + c * 32, v + c * 32);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[ab]);
       const int k = tile / p.tiles_per_head, row = (tile % p.tiles_per_head) * 128 + m;
       if (row >= p.R) continue;
 #pragma unroll
-      for (int b = 0; b < 64; ++b) {
-        if (b >= p.Bp) break;
-        const float zsum = v[b] + v[p.Bp + b];
+      for (int b = 0; b < BP; ++b) {
+        const float zsum = v[b] + v[BP + b];
         if (p.first) {
           float val = 0.f;
           if (b < p.B) val = zsum / (1.f + expf(-zsum)) + bf16_bits_to_f32(p.h[(size_t)b * p.H + row]);
           const uint32_t hi = f32_to_bf16_bits(val);
           const uint32_t lo = f32_to_bf16_bits(val - bf16_bits_to_f32(hi));
           p.u2[((size_t)k * p.N + b) * p.H + row] = (uint16_t)hi;
-          p.u2[((size_t)k * p.N + p.Bp + b) * p.H + row] = (uint16_t)lo;
+          p.u2[((size_t)k * p.N + BP + b) * p.H + row] = (uint16_t)lo;
         } else if (b < p.B) {
           p.z[((size_t)b * p.K + k) * p.R + row] = zsum;
         }
@@ -233,7 +233,7 @@ static bool map_rows(CUtensorMap* m, const void* base, int H, long long rows, in
 int heads_tc_bp(int B) { return (B + 15) / 16 * 16; }
 
 bool heads_tc_supported(int B, int H, const void* h, const void* w1, const void* w2) {
-  return B >= 8 && B <= 64 && H % 64 == 0 && H >= 64 && aligned16(h) && aligned16(w1) && aligned16(w2) &&
+  return B >= 4 && B <= 64 && H % 64 == 0 && H >= 64 && aligned16(h) && aligned16(w1) && aligned16(w2) &&
          heads_encode_fn() != nullptr;
 }
 
@@ -246,10 +246,16 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   if (!map_rows(&ma1, w1, H, (long long)K * H, 128) || !map_rows(&mb1, h, H, B, N) ||
       !map_rows(&ma2, w2, H, (long long)K * V, 128) || !map_rows(&mb2, u2, H, (long long)K * N, N))
     return MEDUSA_ERR_CUDA;
-  if (cudaFuncSetAttribute(heads_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)htc::kSmemBytes) !=
-      cudaSuccess)
+  auto kern = Bp == 16 ? heads_tc_kernel<16> : Bp == 32 ? heads_tc_kernel<32> : Bp == 48 ? heads_tc_kernel<48>
+                                                                                 : heads_tc_kernel<64>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)htc::kSmemBytes) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
   const int sms = device_sm_count();
+  // Equal-cost tiles: as many rounds as the SM count forces, spread evenly.
+  auto grid_for = [&](int tiles) {
+    const int rounds = (tiles + sms - 1) / sms;
+    return (tiles + rounds - 1) / rounds;
+  };
   htc::Params p{};
   p.K = K;
   p.H = H;
@@ -265,13 +271,13 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   p.first = 1;
   p.tiles_per_head = ceil_div(H, 128);
   p.tiles = K * p.tiles_per_head;
-  heads_tc_kernel<<<p.tiles < sms ? p.tiles : sms, htc::kThreads, htc::kSmemBytes, s>>>(ma1, mb1, p);
+  kern<<<grid_for(p.tiles), htc::kThreads, htc::kSmemBytes, s>>>(ma1, mb1, p);
   // W2: rows per head = V
   p.R = V;
   p.first = 0;
   p.tiles_per_head = ceil_div(V, 128);
   p.tiles = K * p.tiles_per_head;
-  heads_tc_kernel<<<p.tiles < sms ? p.tiles : sms, htc::kThreads, htc::kSmemBytes, s>>>(ma2, mb2, p);
+  kern<<<grid_for(p.tiles), htc::kThreads, htc::kSmemBytes, s>>>(ma2, mb2, p);
   return launch_status();
 }
 

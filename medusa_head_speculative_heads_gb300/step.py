@@ -104,7 +104,7 @@ class VerifyStep:
         """Kernels the five calls launch (mirrors the library's dispatch)."""
         import torch
         B, V = self.dims["B"], self.dims["V"]
-        if B >= 8 and self.dtype == torch.bfloat16 and self.dims["H"] % 64 == 0:
+        if B >= 4 and self.dtype == torch.bfloat16 and self.dims["H"] % 64 == 0:
             heads = 2 + (2 if V > 4096 else 1)  # tensor-core W1, W2, then the top-k of z
         else:
             heads = 2 * (-(-B // 8))  # W1 and W2 per pass of <= 8 rows; the W2 pass merges the top-k
