@@ -17,13 +17,17 @@
 // kv head and 128 keys.
 //
 // Roles (256 threads): warp 0 lane 0 issues TMA (Q once per item; K and V of
-// every key tile into a five-slot ring of 32 KB half-tiles, a K slot freed as
-// soon as its S = Q K^T is done, a V slot when its P V is done); warp 1 allocates TMEM and lane 0 issues the MMAs
-// (S = Q K^T into one of two S buffers, O += P V); warps 4-7 (one row per
+// every key tile into a six-slot ring of 32 KB half-tiles, a K slot freed as
+// soon as its S = Q K^T is done, a V slot when its P V is done); warp 1
+// allocates TMEM and lane 0 issues the MMAs (S = Q K^T into one of two S
+// buffers, O += P V with P read from tensor memory); warps 4-7 (one row per
 // thread) read S from TMEM, apply the prefix-length / ancestor mask, keep the
 // online softmax in the log2 domain (O is rescaled in TMEM only when the row
-// maximum grows by more than 2^8), write P (bf16) to shared memory and finally
-// normalise O and store the output.  Every wait is bounded: a timeout sets
+// maximum grows by more than 2^8), write P (bf16 pairs) into one of two TMEM P
+// buffers and finally normalise O and store the output.  With P double
+// buffered, the probabilities of tile t+1 wait only for the P V of tile t-1
+// (and for that of tile t only when O has to be rescaled), so the V slots are
+// released early and more of the ring stays in flight.  Every wait is bounded: a timeout sets
 // MEDUSA_DEV_TIMEOUT, all roles stop, outstanding copies and MMAs are waited
 // for and TMEM is freed before the kernel returns.
 #include <cuda.h>
@@ -39,17 +43,17 @@ using namespace sm100;
 namespace tc {
 
 constexpr int kThreads = 256;
-constexpr int kSlots = 5;                               // ring of K or V half-tiles
+constexpr int kSlots = 6;                               // ring of K or V half-tiles
 constexpr uint32_t kHalf = 16384;                       // 128 rows x 128 bytes
 constexpr uint32_t kBox = 8192;                         // 64 rows x 128 bytes
 constexpr uint32_t kOffQ = 0;                           // 2 d-halves
 constexpr uint32_t kOffRing = 2 * kHalf;                // slot = K or V of one tile (2 d-halves)
 constexpr uint32_t kSlotBytes = 2 * kHalf;
-constexpr uint32_t kOffP = kOffRing + kSlots * kSlotBytes;  // 2 key-halves
-constexpr uint32_t kOffBar = kOffP + 2 * kHalf;
+constexpr uint32_t kOffBar = kOffRing + kSlots * kSlotBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;                     // S0, S1 (128 each), O (128)
+constexpr uint32_t kTmemCols = 512;                     // S0, S1, O (128 each), P0, P1 (64 each)
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;                         // P buffer b at kColP + 64 b (bf16 pairs)
 constexpr uint64_t kWaitNs = 1000000000ull;             // 1 s per wait
 constexpr uint64_t kDrainNs = 100000000ull;             // 100 ms per drain wait
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
@@ -71,7 +75,7 @@ struct Params {
 
 struct Bars {
   uint64_t full[kSlots], empty[kSlots];
-  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full, o_done, o_free, drain;
+  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_free, drain;
 };
 
 // Half-tile c of the load sequence: K of tile g is c = 2g, V of tile g is 2g + 1.
@@ -145,9 +149,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->s_free[s], 128);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->pv_done[s], 1);
     }
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     fence_mbar_init();
@@ -162,14 +166,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tma_prefetch(&tm_vc);
     tma_prefetch(&tm_kt);
     tma_prefetch(&tm_vt);
-  }
-  // Packed tiles: each row's P columns outside its own head block stay zero.
-  if (PACKED && warp >= 4) {
-    const int m = threadIdx.x - 128, other = 1 - (m >> 6);
-    uint4 z = make_uint4(0, 0, 0, 0);
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(smem + kOffP + other * kHalf + m * 128 + c * 16) = z;
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -224,7 +220,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    int g = 0, n = 0, pv = 0;
+    int g = 0, n = 0;
     bool alive = true;
     for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
       const Item x = decode(p, it);
@@ -259,7 +255,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (j >= 1) {
           const int t = j - 1, gt = g0 + t, cv = 2 * gt + 1;
           if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
-          if (!(alive = warp_wait(&bars->p_full, pv & 1, &s_abort))) break;
+          if (!(alive = warp_wait(&bars->p_full[gt & 1], (gt >> 1) & 1, &s_abort))) break;
           if (!(alive = warp_wait(&bars->full[slot_of(cv)], use_parity(cv), &s_abort))) break;
           uint8_t* vb = smem + kOffRing + slot_of(cv) * kSlotBytes;
           // The last prefix tile may run past prefix_len: zero those V rows
@@ -278,18 +274,17 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t pa = smem_u32(smem + kOffP);
+            const uint32_t pa = tmem + kColP + 64 * (gt & 1);
             const uint32_t va = smem_u32(vb);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              mma_bf16(tmem + kColO, smem_desc_sw128(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                       smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, (kk > 0 || t > 0) ? 1u : 0u);
+              mma_bf16_ts(tmem + kColO, pa + 8 * kk, smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
+                          (kk > 0 || t > 0) ? 1u : 0u);
             }
-            mma_commit(&bars->o_done);
+            mma_commit(&bars->pv_done[gt & 1]);
             mma_commit(&bars->empty[slot_of(cv)]);
           }
           __syncwarp();
-          ++pv;
         }
       }
       g = g0 + x.T;
@@ -306,7 +301,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int slot = PACKED ? (m >> 6) : 0;          // warp-uniform
     constexpr int ncol = PACKED ? 64 : 128;
     const int col0 = PACKED ? 64 * slot : 0;
-    int g = 0, pv = 0;
+    // Packed tiles: each row's P columns outside its own head block stay zero.
+    if (PACKED) {
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+      for (int b = 0; b < 2; ++b) tmem_st32u(lane_addr + kColP + 64 * b + 32 * (1 - slot), z);
+      tmem_wait_st();
+    }
+    int g = 0;
     bool alive = true;
     for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
       const Item x = decode(p, it);
@@ -376,40 +379,36 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           pk[c >> 1] = pack_bf16x2(a, b2);
         }
         l = l * f + rs;
-        if (t > 0) {
-          // PV of the previous tile must be done before O is touched or P rewritten.
-          if (!(alive = warp_wait(&bars->o_done, pv & 1, &s_abort))) break;
-          ++pv;
+        if (t > 0 && __any_sync(0xffffffffu, need)) {
+          // O is rescaled only after the previous tile's PV has landed in it.
+          const int gp = g - 1;
+          if (!(alive = warp_wait(&bars->pv_done[gp & 1], (gp >> 1) & 1, &s_abort))) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {
-            float o[32];
+          float o[32];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              tmem_ld32(lane_addr + kColO + 32 * c4, o);
-              tmem_wait_ld();
+          for (int c4 = 0; c4 < 4; ++c4) {
+            tmem_ld32(lane_addr + kColO + 32 * c4, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= f;
-              tmem_st32(lane_addr + kColO + 32 * c4, o);
-            }
-            tmem_wait_st();
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tmem_st32(lane_addr + kColO + 32 * c4, o);
           }
         }
-        uint8_t* prow = smem + kOffP + m * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < ncol / 8; ++c8) {
-          const int kc = (col0 >> 6) + (c8 >> 3);  // key half (P region)
-          const int chunk = c8 & 7;
-          *reinterpret_cast<uint4*>(prow + kc * kHalf + ((chunk ^ (m & 7)) << 4)) =
-              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        // P buffer g & 1 is free once the PV of tile g - 2 has read it.
+        const int pb = g & 1;
+        if (g >= 2) {
+          if (!(alive = warp_wait(&bars->pv_done[pb], ((g - 2) >> 1) & 1, &s_abort))) break;
+          tc_fence_after();
         }
-        fence_proxy_async_smem();
+        tmem_st32u(lane_addr + kColP + 64 * pb + (PACKED ? 32 * slot : 0), pk);
+        if constexpr (!PACKED) tmem_st32u(lane_addr + kColP + 64 * pb + 32, pk + 32);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[pb]);
       }
       if (!alive) break;
-      // Epilogue: O / l -> bf16 output row.
-      if (!(alive = warp_wait(&bars->o_done, pv & 1, &s_abort))) break;
-      ++pv;
+      // Epilogue: O / l -> bf16 output row, after the item's last PV.
+      if (!(alive = warp_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &s_abort))) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint16_t* orow = p.out + ((((size_t)x.lb * p.N + (row_ok ? node : 0)) * p.Hq) + (size_t)h * p.G + gq) * 128;

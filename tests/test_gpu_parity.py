@@ -201,6 +201,34 @@ def test_tree_attention_ignores_rows_past_prefix(mg):
     assert rel_err(o, ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("Hq,Hkv,tree", [(4, 4, ("dense", (2, 2, 2), 15)), (8, 2, ("greedy", 10, 64))],
+                         ids=["two-heads-per-tile", "128-row-tiles"])
+def test_tree_attention_scores_growing_over_tiles(mg, Hq, Hkv, tree):
+    """Key blocks scaled up along the prefix (x4, then x8; tree keys x2), so a
+    row's running maximum grows by far more than 2^8 after its first tiles and
+    the accumulated output has to be rescaled mid-row."""
+    c = wl.config("tiny", dtype="bf16", nl=1, B=2, Hq=Hq, Hkv=Hkv, d=128, L=300, tree=tree)
+    t = _topo(c)
+    N = t.n_nodes
+    pl = np.array([300, 250], np.int32)
+    q = wl.queries(c, N)
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    kf = wl.bf16_bits_to_f32(kc)
+    kf[:, :, 64:128] *= 4.0
+    kf[:, :, 192:256] *= 8.0
+    kc = wl.to_bf16_bits(kf)
+    kt = wl.to_bf16_bits(wl.bf16_bits_to_f32(kt) * 2.0)
+    _, _, mask = otopo.tree_build(t, np.zeros(2, np.int32), np.zeros((2, max(1, t.max_depth), 10), np.int32), pl)
+    ref = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    st = _status(mg)
+    out = mg.medusa_tree_attention(to_dev(q), to_dev(kc), to_dev(vc), to_dev(kt), to_dev(vt),
+                                   to_dev(mask.view(np.int32)), to_dev(pl), d_status=st)
+    torch.cuda.synchronize()
+    assert rel_err(bf16_to_f64(to_host(out)), ref) <= TOL["bf16"]
+    assert mg.medusa_status_check(st) == 0
+
+
 def test_tree_attention_bad_prefix_len_reports(mg):
     c = wl.config("tiny", nl=1, B=1, Hq=2, Hkv=2, d=64, L=16)
     t = otopo.dense([2])
