@@ -166,7 +166,7 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
                    int32_t* __restrict__ accept_len, int32_t* __restrict__ path_nodes,
                    int32_t* __restrict__ next_tok, float* __restrict__ p_tok, float* __restrict__ thr_out,
                    int32_t* d_status) {
-  __shared__ int acc[MEDUSA_MAX_NODES], pass[MEDUSA_MAX_NODES], amax[MEDUSA_MAX_NODES];
+  __shared__ int acc[MEDUSA_MAX_NODES], pass[MEDUSA_MAX_NODES], amax[MEDUSA_MAX_NODES], par[MEDUSA_MAX_NODES];
   __shared__ float zmax[MEDUSA_MAX_NODES], ssum[MEDUSA_MAX_NODES], thr[MEDUSA_MAX_NODES];
   __shared__ int s_key[kSelectThreads / 32];
   __shared__ int s_bad;
@@ -180,6 +180,7 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
     int a = INT_MAX;
     if (node < N) {
       const float4* pp = part + ((size_t)b * N + node) * C;
+#pragma unroll 4
       for (int k = sub; k < C; k += grp) {
         const float4 q = pp[k];
         combine_stats(m, a, S, E, q.x, __float_as_int(q.y), q.z, q.w, inv_t);
@@ -214,6 +215,7 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
     pc = parent[c];
     if (c > 0 && (pc < 0 || pc >= c || dc < 1 || dc > max_depth)) s_bad = 1;
     acc[c] = c == 0 ? 1 : 0;
+    par[c] = pc;
   }
   __syncthreads();
   if (s_bad) {
@@ -269,7 +271,7 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
     int a = best;
     for (int j = db; j >= 0; --j) {
       pn[j] = a;
-      a = j ? parent[a] : -1;
+      a = j ? par[a] : -1;  // the walk stays in shared memory
     }
     accept_len[b] = db + 1;
     next_tok[b] = amax[best];

@@ -15,11 +15,13 @@
 // the regular top-k kernels then rank.
 //
 // Roles (256 threads, one CTA per SM, persistent over 128-row tiles): warp 0
-// lane 0 issues TMA loads of the A (weights) and B (vector) tiles into a
-// six-stage ring; warp 1 allocates TMEM and lane 0 issues the MMAs (four
-// K=16 steps per 64-column stage) into one of two accumulators; warps 4-7
-// read the accumulator (one row per thread) and write the outputs, so the
-// epilogue of one tile overlaps the main loop of the next.  Every wait is
+// lane 0 issues TMA loads of the A (weights) and B (vector) tiles into a ring
+// of 6 to 10 stages (the smaller the batch, the smaller the B tile and the
+// more weight bytes in flight); warp 1 allocates TMEM and lane 0 issues the
+// MMAs (four K=16 steps per 64-column stage) into one of two accumulators;
+// warps 4-7 read the accumulator (one row per thread) and write the outputs,
+// so the epilogue of one tile overlaps the main loop of the next.  The W1
+// epilogue's residual h values are loaded before the accumulator wait.  Every wait is
 // bounded; a timeout sets MEDUSA_DEV_TIMEOUT and the kernel drains its
 // copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -35,13 +37,21 @@ using namespace sm100;
 namespace htc {
 
 constexpr int kThreads = 256;
-constexpr int kStages = 6;
+constexpr int kMaxStages = 10;
 constexpr uint32_t kATile = 16384;  // 128 rows x 128 bytes
-constexpr uint32_t kBTile = 16384;  // up to 128 rows x 128 bytes
-constexpr uint32_t kStageBytes = kATile + kBTile;
-constexpr uint32_t kOffBar = kStages * kStageBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
+
+// Ring geometry for a padded batch BP: the B tile holds 2 BP rows of 128 bytes.
+template <int BP>
+struct Ring {
+  static constexpr uint32_t kStageBytes = kATile + 256u * BP;
+  static constexpr int kStages = (int)(200u * 1024u / kStageBytes) < kMaxStages ? (int)(200u * 1024u / kStageBytes)
+                                                                                 : kMaxStages;
+  static constexpr uint32_t kOffBar = kStages * kStageBytes;
+  static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+  static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -56,7 +66,7 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
+  uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2], drain;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -72,6 +82,9 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                 const htc::Params p) {
   constexpr int NC = 2 * BP;  // accumulator columns
   using namespace htc;
+  constexpr int kStages = Ring<BP>::kStages;
+  constexpr uint32_t kStageBytes = Ring<BP>::kStageBytes;
+  constexpr uint32_t kOffBar = Ring<BP>::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
@@ -167,6 +180,17 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     int tc = 0;
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tc) {
       const int ab = tc & 1;
+      // W1: this row's residual h[b][row] (bf16 pairs), loaded while the MMAs run.
+      uint32_t hres[BP / 2];
+      if (p.first) {
+        const int row = (tile % p.tiles_per_head) * 128 + m;
+#pragma unroll
+        for (int b2 = 0; b2 < BP / 2; ++b2) {
+          const uint32_t lo = (2 * b2 < p.B && row < p.R) ? __ldg(p.h + (size_t)(2 * b2) * p.H + row) : 0u;
+          const uint32_t hi = (2 * b2 + 1 < p.B && row < p.R) ? __ldg(p.h + (size_t)(2 * b2 + 1) * p.H + row) : 0u;
+          hres[b2] = lo | (hi << 16);
+        }
+      }
       if (!warp_wait(&bars->acc_full[ab], (tc >> 1) & 1, &s_abort)) break;
       tc_fence_after();
       float v[NC];
@@ -182,7 +206,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         const float zsum = v[b] + v[BP + b];
         if (p.first) {
           float val = 0.f;
-          if (b < p.B) val = zsum / (1.f + expf(-zsum)) + bf16_bits_to_f32(p.h[(size_t)b * p.H + row]);
+          if (b < p.B) val = zsum / (1.f + expf(-zsum)) + bf16_bits_to_f32((hres[b >> 1] >> (16 * (b & 1))) & 0xffffu);
           const uint32_t hi = f32_to_bf16_bits(val);
           const uint32_t lo = f32_to_bf16_bits(val - bf16_bits_to_f32(hi));
           p.u2[((size_t)k * p.N + b) * p.H + row] = (uint16_t)hi;
@@ -248,7 +272,11 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
     return MEDUSA_ERR_CUDA;
   auto kern = Bp == 16 ? heads_tc_kernel<16> : Bp == 32 ? heads_tc_kernel<32> : Bp == 48 ? heads_tc_kernel<48>
                                                                                  : heads_tc_kernel<64>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)htc::kSmemBytes) != cudaSuccess)
+  const uint32_t smem = Bp == 16   ? htc::Ring<16>::kSmemBytes
+                        : Bp == 32 ? htc::Ring<32>::kSmemBytes
+                        : Bp == 48 ? htc::Ring<48>::kSmemBytes
+                                   : htc::Ring<64>::kSmemBytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
   const int sms = device_sm_count();
   // Equal-cost tiles: as many rounds as the SM count forces, spread evenly.
@@ -271,13 +299,13 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   p.first = 1;
   p.tiles_per_head = ceil_div(H, 128);
   p.tiles = K * p.tiles_per_head;
-  kern<<<grid_for(p.tiles), htc::kThreads, htc::kSmemBytes, s>>>(ma1, mb1, p);
+  kern<<<grid_for(p.tiles), htc::kThreads, smem, s>>>(ma1, mb1, p);
   // W2: rows per head = V
   p.R = V;
   p.first = 0;
   p.tiles_per_head = ceil_div(V, 128);
   p.tiles = K * p.tiles_per_head;
-  kern<<<grid_for(p.tiles), htc::kThreads, htc::kSmemBytes, s>>>(ma2, mb2, p);
+  kern<<<grid_for(p.tiles), htc::kThreads, smem, s>>>(ma2, mb2, p);
   return launch_status();
 }
 

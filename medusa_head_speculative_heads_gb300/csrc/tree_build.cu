@@ -26,18 +26,22 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
                   int32_t* __restrict__ pos, uint32_t* __restrict__ mask, int32_t* d_status) {
   __shared__ int s_parent[MEDUSA_MAX_NODES], s_depth[MEDUSA_MAX_NODES];
   const int b = blockIdx.x, n = threadIdx.x;
+  // Every independent load first (one round trip), then the top-k gather.
+  int rk = 0, L = 0, tok0 = 0;
   if (n < N) {
     s_parent[n] = parent[n];
     s_depth[n] = depth[n];
+    rk = rank[n];
+    L = prefix_len[b];
+    if (n == 0) tok0 = root_tok[b];
   }
   __syncthreads();
   if (n >= N) return;
   const int dn = s_depth[n];
   int tok;
   if (n == 0) {
-    tok = root_tok[b];
+    tok = tok0;
   } else {
-    const int rk = rank[n];
     if (dn < 1 || dn > K || rk < 0 || rk >= topk) {
       set_status(d_status, MEDUSA_DEV_BAD_INDEX);
       tok = -1;
@@ -46,7 +50,7 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
     }
   }
   tokens[(size_t)b * N + n] = tok;
-  pos[(size_t)b * N + n] = prefix_len[b] + dn;
+  pos[(size_t)b * N + n] = L + dn;
 
   if (b == 0) {
     const int W = (N + 31) / 32;
