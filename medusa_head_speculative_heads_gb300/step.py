@@ -113,3 +113,73 @@ class VerifyStep:
 
     def check(self, stream=None) -> int:
         return B_.medusa_status_check(self.status, stream)
+
+
+class PipelinedSteps:
+    """Verify steps fed from host memory, with the host->device copy of the
+    next step's inputs overlapping the current step's kernels.
+
+    Two device copies of the per-step inputs alternate: step i runs (as a
+    captured graph, followed by the device->host read of its results) on the
+    compute stream from set i % 2 while a copy stream uploads step i + 1's
+    inputs into the other set, which step i - 1 has finished reading.  Model
+    state (weights, KV cache) stays resident and is shared by both sets.
+
+    `dev_inputs` maps the per-step input names (h, root_tok, prefix_len, q, kt,
+    vt, logits) to device tensors (set 0; set 1 is allocated alike);
+    `resident` holds w1, w2, kc, vc; `outs` are device results read back into
+    `host_outs` (pinned) at the end of every step."""
+
+    names = ("h", "root_tok", "prefix_len", "q", "kt", "vt", "logits")
+
+    def __init__(self, vs: VerifyStep, dev_inputs: dict, resident: dict, outs, host_outs):
+        import torch
+        self.vs = vs
+        self.sets = [dict(dev_inputs), {k: torch.empty_like(dev_inputs[k]) for k in self.names}]
+        for k in self.names:
+            self.sets[1][k].copy_(dev_inputs[k])
+        self.outs, self.host_outs = list(outs), list(host_outs)
+        self.copy_stream = torch.cuda.Stream()
+        self.copied = [torch.cuda.Event(), torch.cuda.Event()]
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        r = resident
+
+        def post():
+            for o, ho in zip(self.outs, self.host_outs):
+                ho.copy_(o, non_blocking=True)
+
+        self.graphs = [vs.capture(s["h"], r["w1"], r["w2"], s["root_tok"], s["prefix_len"], s["q"], r["kc"], r["vc"],
+                                  s["kt"], s["vt"], s["logits"], post=post) for s in self.sets]
+        self.i = 0
+
+    def bytes_h2d(self) -> int:
+        return sum(self.sets[0][k].numel() * self.sets[0][k].element_size() for k in self.names)
+
+    def bytes_d2h(self) -> int:
+        return sum(o.numel() * o.element_size() for o in self.outs)
+
+    def step(self, host_inputs: dict):
+        """Enqueues one step whose inputs are the pinned host tensors `host_inputs`
+        (no host synchronisation)."""
+        import torch
+        s = self.i % 2
+        main = torch.cuda.current_stream()
+        cs = self.copy_stream
+        if self.i == 0:
+            cs.wait_stream(main)  # a new sequence starts after everything enqueued so far
+        with torch.cuda.stream(cs):
+            if self.i >= 2:
+                cs.wait_event(self.done[s])  # step i - 2 has finished reading this set
+            for k in self.names:
+                self.sets[s][k].copy_(host_inputs[k], non_blocking=True)
+            self.copied[s].record(cs)
+        main.wait_event(self.copied[s])
+        self.graphs[s].replay()
+        self.done[s].record(main)
+        self.i += 1
+
+    def reset(self):
+        """Starts a new sequence (the next step waits for nothing earlier)."""
+        import torch
+        torch.cuda.synchronize()
+        self.i = 0

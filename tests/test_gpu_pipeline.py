@@ -1,0 +1,83 @@
+"""PipelinedSteps: verify steps fed from pinned host memory, the upload of
+step i + 1's inputs overlapping step i's kernels (two device input sets).
+
+Four steps with different inputs are enqueued back to back with no host
+synchronisation.  Their prefix lengths grow by 2 per step, so every step's
+attention reads cache rows that the previous step's compaction wrote: a step
+that ran out of order or read the other input set changes the result.  The
+final results and the whole KV cache must equal those of the same four steps
+run one after another."""
+import numpy as np
+import pytest
+
+import workloads as wl
+from tests.helpers import to_dev, to_host
+from tests.step import lib_topology, make_step_inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+PER_STEP = ("h", "root_tok", "prefix_len", "q", "kt", "vt", "logits")
+
+
+@pytest.fixture(scope="module")
+def mg():
+    import medusa_head_speculative_heads_gb300 as m
+    m.build()
+    return m
+
+
+def _steps(c, n):
+    L0 = c["L"] - 8
+    steps = []
+    for k in range(n):
+        inp = make_step_inputs(c, rows=[k])
+        inp["prefix_len"] = np.array([L0 + 2 * k], np.int32)
+        steps.append(inp)
+    return steps
+
+
+def _verify_step(mg, c):
+    from medusa_head_speculative_heads_gb300.step import VerifyStep
+    return VerifyStep(B=1, H=c["H"], V=c["V"], K=c["K"], topk=c["topk"], nl=c["nl"], Hq=c["Hq"], Hkv=c["Hkv"],
+                      d=c["d"], Lmax=c["Lmax"], dtype=torch.float32, topology=lib_topology(mg, c),
+                      temperature=c["T"], eps=c["eps"], delta=c["delta"])
+
+
+def test_pipelined_steps_match_sequential_steps(mg):
+    from medusa_head_speculative_heads_gb300.step import PipelinedSteps
+    c = wl.config("tiny")
+    steps = _steps(c, 4)
+    w1, w2 = to_dev(steps[0]["w1"]), to_dev(steps[0]["w2"])
+
+    # one step after another (eager, no overlap)
+    vs = _verify_step(mg, c)
+    kc, vc = to_dev(steps[0]["kc"]), to_dev(steps[0]["vc"])
+    for inp in steps:
+        d = {k: to_dev(inp[k]) for k in PER_STEP}
+        vs.run(d["h"], w1, w2, d["root_tok"], d["prefix_len"], d["q"], kc, vc, d["kt"], d["vt"], d["logits"])
+        torch.cuda.synchronize()
+    assert vs.check() == 0
+    ref = dict(accept_len=to_host(vs.accept_len), path_nodes=to_host(vs.path_nodes), next_tok=to_host(vs.next_tok),
+               new_len=to_host(vs.new_len), attn_out=to_host(vs.attn_out), kc=to_host(kc), vc=to_host(vc))
+    assert ref["new_len"][0] > steps[-1]["prefix_len"][0]
+
+    # pipelined: host inputs, uploads overlapping the previous step
+    vs2 = _verify_step(mg, c)
+    kc2, vc2 = to_dev(steps[0]["kc"]), to_dev(steps[0]["vc"])
+    outs = [vs2.accept_len, vs2.path_nodes, vs2.next_tok, vs2.new_len]
+    host_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    pipe = PipelinedSteps(vs2, {k: to_dev(steps[0][k]) for k in PER_STEP}, dict(w1=w1, w2=w2, kc=kc2, vc=vc2),
+                          outs, host_outs)
+    hosts = [{k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory() for k in PER_STEP} for inp in steps]
+    pipe.reset()
+    for hst in hosts:
+        pipe.step(hst)
+    torch.cuda.synchronize()
+    assert vs2.check() == 0
+    assert pipe.bytes_h2d() == sum(hosts[0][k].numel() * hosts[0][k].element_size() for k in PER_STEP)
+    for name, ho in zip(("accept_len", "path_nodes", "next_tok", "new_len"), host_outs):
+        np.testing.assert_array_equal(ho.numpy(), ref[name], err_msg=name)
+    np.testing.assert_array_equal(to_host(vs2.attn_out), ref["attn_out"])
+    np.testing.assert_array_equal(to_host(kc2), ref["kc"])
+    np.testing.assert_array_equal(to_host(vc2), ref["vc"])
