@@ -78,16 +78,17 @@ struct Bars {
   uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_free, drain;
 };
 
-// Half-tiles are loaded in the order the MMAs consume them, so the ring is a
-// strict FIFO and a V tile arrives when its PV is due instead of sitting in a
-// slot while the softmax of its tile runs: per item of T key tiles the
-// sequence is K0, K1, V0, K2, V1, ..., K(T-1), V(T-2), V(T-1).  Half-tile c of
-// the whole sequence (items back to back, 2T half-tiles each) uses ring slot
-// c % kSlots.
+// The MMA warp issues, for j = 0 .. T + kLag - 1, S(j) = Q K(j)^T (j < T) and
+// then O += P(j - kLag) V(j - kLag) (j >= kLag): the PVs trail the score
+// products by kLag tiles, so S(j + 1) never waits behind the PV of the tile
+// whose softmax has just finished, and the softmax warps find the next S
+// ready.  The producer loads the half-tiles in exactly that order (K(j), then
+// V(j - kLag)), so the ring is a strict FIFO and a V tile lands when its PV is
+// due.  Half-tile c of the whole sequence (items back to back, 2T each) uses
+// ring slot c % kSlots.
+constexpr int kLag = 2;
 __device__ __forceinline__ int slot_of(int c) { return c % kSlots; }
 __device__ __forceinline__ uint32_t use_parity(int c) { return (uint32_t)(c / kSlots) & 1u; }
-__device__ __forceinline__ int seq_k(int t) { return t == 0 ? 0 : 2 * t - 1; }          // position of K(t)
-__device__ __forceinline__ int seq_v(int t, int T) { return t == T - 1 ? 2 * T - 1 : 2 * t + 2; }  // of V(t)
 
 struct Item {
   int lb, b, h0, mt, L, T, n_pre;
@@ -198,26 +199,26 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tma_load_5d(smem + kOffQ + dh * kHalf, &tm_q, &bars->q_full, 64 * dh, 0, x.h0, x.mt * (128 / p.G), x.lb);
           }
         }
-        for (int q = 0; q < 2 * x.T && alive; ++q) {
-          // position q -> (key tile t, K or V), the inverse of seq_k / seq_v
-          int t, kv;
-          if (q == 0) { t = 0; kv = 0; }
-          else if (q == 2 * x.T - 1) { t = x.T - 1; kv = 1; }
-          else if (q & 1) { t = (q + 1) >> 1; kv = 0; }
-          else { t = (q - 2) >> 1; kv = 1; }
-          const bool tree = t >= x.n_pre;
-          const int j0 = (tree ? t - x.n_pre : t) * p.KT;
-          const int c = 2 * g + q, sl = slot_of(c);
-          if (c >= kSlots && !(alive = mbar_wait_bounded(&bars->empty[sl], use_parity(c - kSlots), &s_abort, kWaitNs)))
-            break;
-          const CUtensorMap* mp = kv ? (tree ? &tm_vt : &tm_vc) : (tree ? &tm_kt : &tm_kc);
-          uint8_t* dst = smem + kOffRing + sl * kSlotBytes;
-          mbar_expect_tx(&bars->full[sl], kSlotBytes);
-          for (int dh = 0; dh < 2; ++dh)
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_4d(dst + dh * kHalf + cb * kBox, mp, &bars->full[sl], 64 * dh,
-                          PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
-          issued = c + 1;
+        int c = 2 * g;  // half-tiles of earlier items: 2T each
+        for (int j = 0; j < x.T + kLag && alive; ++j) {
+          for (int kv = 0; kv < 2 && alive; ++kv) {
+            const int t = kv ? j - kLag : j;  // K(j), then V(j - kLag)
+            if (t < 0 || t >= x.T) continue;
+            const bool tree = t >= x.n_pre;
+            const int j0 = (tree ? t - x.n_pre : t) * p.KT;
+            const int sl = slot_of(c);
+            if (c >= kSlots &&
+                !(alive = mbar_wait_bounded(&bars->empty[sl], use_parity(c - kSlots), &s_abort, kWaitNs)))
+              break;
+            const CUtensorMap* mp = kv ? (tree ? &tm_vt : &tm_vc) : (tree ? &tm_kt : &tm_kc);
+            uint8_t* dst = smem + kOffRing + sl * kSlotBytes;
+            mbar_expect_tx(&bars->full[sl], kSlotBytes);
+            for (int dh = 0; dh < 2; ++dh)
+              for (int cb = 0; cb < 2; ++cb)
+                tma_load_4d(dst + dh * kHalf + cb * kBox, mp, &bars->full[sl], 64 * dh,
+                            PACKED ? x.h0 + cb : x.h0, PACKED ? j0 : j0 + 64 * cb, x.lb);
+            issued = ++c;
+          }
         }
         g += x.T;
       }
@@ -242,9 +243,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       if (!(alive = warp_wait(&bars->q_full, n & 1, &s_abort))) break;
       tc_fence_after();
       const int g0 = g;
-      for (int j = 0; j <= x.T && alive; ++j) {
+      int c = 2 * g0;  // next half-tile of the load sequence
+      for (int j = 0; j < x.T + kLag && alive; ++j) {
         if (j < x.T) {
-          const int gj = g0 + j, ck = 2 * g0 + seq_k(j), sb = gj & 1;
+          const int gj = g0 + j, ck = c++, sb = gj & 1;
           if (!(alive = warp_wait(&bars->full[slot_of(ck)], use_parity(ck), &s_abort))) break;
           if (gj >= 2 && !(alive = warp_wait(&bars->s_free[sb], ((gj >> 1) - 1) & 1, &s_abort))) break;
           tc_fence_after();
@@ -263,8 +265,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           }
           __syncwarp();
         }
-        if (j >= 1) {
-          const int t = j - 1, gt = g0 + t, cv = 2 * g0 + seq_v(t, x.T);
+        if (j >= kLag) {
+          const int t = j - kLag, gt = g0 + t, cv = c++;
           if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
           if (!(alive = warp_wait(&bars->p_full[gt & 1], (gt >> 1) & 1, &s_abort))) break;
           if (!(alive = warp_wait(&bars->full[slot_of(cv)], use_parity(cv), &s_abort))) break;
