@@ -226,12 +226,22 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
       for (int bb = 0; bb < BB; ++bb)
         if (lane == ((i * BB + bb) & 31)) emit(r + i, bb, acc[i][bb]);
   }
-  for (; r < w_hi; ++r) {
-    float acc[1][BB];
-    warp_rows<TW, BB, 1>(Wk + (size_t)r * C, C, xs, lane, acc);
+  // The remaining 1-3 rows in one pass (their loads in flight together).
+  auto tail = [&](auto nr) {
+    constexpr int NR = decltype(nr)::value;
+    float acc[NR][BB];
+    warp_rows<TW, BB, NR>(Wk + (size_t)r * C, C, xs, lane, acc);
 #pragma unroll
-    for (int bb = 0; bb < BB; ++bb)
-      if (lane == (bb & 31)) emit(r, bb, acc[0][bb]);
+    for (int i = 0; i < NR; ++i)
+#pragma unroll
+      for (int bb = 0; bb < BB; ++bb)
+        if (lane == ((i * BB + bb) & 31)) emit(r + i, bb, acc[i][bb]);
+  };
+  switch (w_hi - r) {
+    case 3: tail(std::integral_constant<int, 3>{}); break;
+    case 2: tail(std::integral_constant<int, 2>{}); break;
+    case 1: tail(std::integral_constant<int, 1>{}); break;
+    default: break;
   }
   if constexpr (!kFirst) {
     __syncthreads();
