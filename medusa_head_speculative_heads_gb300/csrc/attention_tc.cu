@@ -19,15 +19,16 @@
 // Roles (256 threads): warp 0 lane 0 issues TMA (Q once per item; K and V of
 // every key tile into a six-slot ring of 32 KB half-tiles, a K slot freed as
 // soon as its S = Q K^T is done, a V slot when its P V is done); warp 1
-// allocates TMEM and lane 0 issues the MMAs (S = Q K^T into one of two S
-// buffers, O += P V with P read from tensor memory); warps 4-7 (one row per
-// thread) read S from TMEM, apply the prefix-length / ancestor mask, keep the
-// online softmax in the log2 domain (O is rescaled in TMEM only when the row
-// maximum grows by more than 2^8), write P (bf16 pairs) into one of two TMEM P
-// buffers and finally normalise O and store the output.  With P double
+// allocates TMEM and lane 0 issues S = Q K^T into one of two S buffers; warp 2
+// lane 0 issues O += P V with P read from tensor memory; warps 4-7 (one row
+// per thread) read S from TMEM, apply the prefix-length / ancestor mask, keep
+// the online softmax in the log2 domain (O is rescaled in TMEM only when the
+// row maximum grows by more than 2^8), write P (bf16 pairs) into one of two
+// TMEM P buffers and finally normalise O and store the output.  With P double
 // buffered, the probabilities of tile t+1 wait only for the P V of tile t-1
-// (and for that of tile t only when O has to be rescaled), so the V slots are
-// released early and more of the ring stays in flight.  Every wait is bounded: a timeout sets
+// (and for that of tile t only when O has to be rescaled), and with the two
+// MMA streams issued by different warps a score product never waits behind a
+// PV.  Every wait is bounded: a timeout sets
 // MEDUSA_DEV_TIMEOUT, all roles stop, outstanding copies and MMAs are waited
 // for and TMEM is freed before the kernel returns.
 #include <cuda.h>
@@ -75,17 +76,15 @@ struct Params {
 
 struct Bars {
   uint64_t full[kSlots], empty[kSlots];
-  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_free, drain;
+  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_free, drain, drain_pv;
 };
 
-// The MMA warp issues, for j = 0 .. T + kLag - 1, S(j) = Q K(j)^T (j < T) and
-// then O += P(j - kLag) V(j - kLag) (j >= kLag): the PVs trail the score
-// products by kLag tiles, so S(j + 1) never waits behind the PV of the tile
-// whose softmax has just finished, and the softmax warps find the next S
-// ready.  The producer loads the half-tiles in exactly that order (K(j), then
-// V(j - kLag)), so the ring is a strict FIFO and a V tile lands when its PV is
-// due.  Half-tile c of the whole sequence (items back to back, 2T each) uses
-// ring slot c % kSlots.
+// Load sequence of one item of T key tiles: for j = 0 .. T + kLag - 1, K(j)
+// (j < T) and then V(j - kLag) (j >= kLag).  The score products run ahead of
+// the PVs, which wait for their tile's softmax, so each V tile is loaded about
+// kLag tiles after its K and lands when its PV is due instead of holding a
+// ring slot.  Both MMA issuers walk this sequence; half-tile c of the whole
+// sequence (items back to back, 2T each) uses ring slot c % kSlots.
 constexpr int kLag = 2;
 __device__ __forceinline__ int slot_of(int c) { return c % kSlots; }
 __device__ __forceinline__ uint32_t use_parity(int c) { return (uint32_t)(c / kSlots) & 1u; }
@@ -162,6 +161,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_pv, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -230,82 +230,95 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           mbar_wait_bounded(&bars->full[slot_of(c)], use_parity(c), nullptr, kDrainNs);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues S = Q K^T for every key tile, warp 2 issues O += P V.  Each
+    // lane 0 commits only its own MMAs, so the score products never queue
+    // behind a PV that is waiting for its softmax, and the tensor pipe takes
+    // both streams.  Both warps walk the same load sequence to find their slots.
+    const bool s_role = warp == 1;
     int g = 0, n = 0;
     bool alive = true;
     for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
       const Item x = decode(p, it);
       if (!x.ok) {
-        if (lane == 0 && x.mt == 0) set_status(p.d_status, MEDUSA_DEV_BAD_LENGTH);
+        if (s_role && lane == 0 && x.mt == 0) set_status(p.d_status, MEDUSA_DEV_BAD_LENGTH);
         continue;
       }
-      if (!(alive = warp_wait(&bars->q_full, n & 1, &s_abort))) break;
-      tc_fence_after();
+      if (s_role) {
+        if (!(alive = warp_wait(&bars->q_full, n & 1, &s_abort))) break;
+        tc_fence_after();
+      }
       const int g0 = g;
       int c = 2 * g0;  // next half-tile of the load sequence
       for (int j = 0; j < x.T + kLag && alive; ++j) {
         if (j < x.T) {
           const int gj = g0 + j, ck = c++, sb = gj & 1;
-          if (!(alive = warp_wait(&bars->full[slot_of(ck)], use_parity(ck), &s_abort))) break;
-          if (gj >= 2 && !(alive = warp_wait(&bars->s_free[sb], ((gj >> 1) - 1) & 1, &s_abort))) break;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t qa = smem_u32(smem + kOffQ);
-            const uint32_t ka = smem_u32(smem + kOffRing + slot_of(ck) * kSlotBytes);
+          if (s_role) {
+            if (!(alive = warp_wait(&bars->full[slot_of(ck)], use_parity(ck), &s_abort))) break;
+            if (gj >= 2 && !(alive = warp_wait(&bars->s_free[sb], ((gj >> 1) - 1) & 1, &s_abort))) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t qa = smem_u32(smem + kOffQ);
+              const uint32_t ka = smem_u32(smem + kOffRing + slot_of(ck) * kSlotBytes);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              mma_bf16(tmem + sb * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                       kIdescQK, kk > 0);
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                mma_bf16(tmem + sb * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                         kIdescQK, kk > 0);
+              }
+              mma_commit(&bars->s_full[sb]);
+              mma_commit(&bars->empty[slot_of(ck)]);
+              if (j == x.T - 1) mma_commit(&bars->q_empty);
             }
-            mma_commit(&bars->s_full[sb]);
-            mma_commit(&bars->empty[slot_of(ck)]);
-            if (j == x.T - 1) mma_commit(&bars->q_empty);
+            __syncwarp();
           }
-          __syncwarp();
         }
         if (j >= kLag) {
           const int t = j - kLag, gt = g0 + t, cv = c++;
-          if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
-          if (!(alive = warp_wait(&bars->p_full[gt & 1], (gt >> 1) & 1, &s_abort))) break;
-          if (!(alive = warp_wait(&bars->full[slot_of(cv)], use_parity(cv), &s_abort))) break;
-          uint8_t* vb = smem + kOffRing + slot_of(cv) * kSlotBytes;
-          // The last prefix tile may run past prefix_len: zero those V rows
-          // (stale cache rows may hold anything, and 0 * NaN is NaN).
-          const int j0 = t * p.KT;
-          if (t < x.n_pre && j0 + p.KT > x.L) {
-            const int first = x.L - j0;  // first invalid key offset within a column block / tile
-            for (int idx = lane; idx < 2 * 128 * 8; idx += 32) {
-              const int dh = idx >> 10, r = (idx >> 3) & 127, c = idx & 7;
-              const int off = PACKED ? (r & 63) : r;
-              if (off >= first)
-                *reinterpret_cast<uint4*>(vb + dh * kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          if (!s_role) {
+            if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
+            if (!(alive = warp_wait(&bars->p_full[gt & 1], (gt >> 1) & 1, &s_abort))) break;
+            if (!(alive = warp_wait(&bars->full[slot_of(cv)], use_parity(cv), &s_abort))) break;
+            uint8_t* vb = smem + kOffRing + slot_of(cv) * kSlotBytes;
+            // The last prefix tile may run past prefix_len: zero those V rows
+            // (stale cache rows may hold anything, and 0 * NaN is NaN).
+            const int j0 = t * p.KT;
+            if (t < x.n_pre && j0 + p.KT > x.L) {
+              const int first = x.L - j0;  // first invalid key offset within a column block / tile
+              for (int idx = lane; idx < 2 * 128 * 8; idx += 32) {
+                const int dh = idx >> 10, r = (idx >> 3) & 127, cc = idx & 7;
+                const int off = PACKED ? (r & 63) : r;
+                if (off >= first)
+                  *reinterpret_cast<uint4*>(vb + dh * kHalf + r * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
             }
-            fence_proxy_async_smem();
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t pa = tmem + kColP + 64 * (gt & 1);
+              const uint32_t va = smem_u32(vb);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                mma_bf16_ts(tmem + kColO, pa + 8 * kk, smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
+                            (kk > 0 || t > 0) ? 1u : 0u);
+              }
+              mma_commit(&bars->pv_done[gt & 1]);
+              mma_commit(&bars->empty[slot_of(cv)]);
+            }
             __syncwarp();
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t pa = tmem + kColP + 64 * (gt & 1);
-            const uint32_t va = smem_u32(vb);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              mma_bf16_ts(tmem + kColO, pa + 8 * kk, smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
-                          (kk > 0 || t > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars->pv_done[gt & 1]);
-            mma_commit(&bars->empty[slot_of(cv)]);
-          }
-          __syncwarp();
         }
       }
       g = g0 + x.T;
       ++n;
     }
     if (!alive && lane == 0) {
-      mma_commit(&bars->drain);
-      mbar_wait_bounded(&bars->drain, 0, nullptr, kDrainNs);
+      // Wait (bounded) for this warp's own MMAs before TMEM is released.
+      uint64_t* d = s_role ? &bars->drain : &bars->drain_pv;
+      mma_commit(d);
+      mbar_wait_bounded(d, 0, nullptr, kDrainNs);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
@@ -446,7 +459,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   }
 
-  if (threadIdx.x == 0 || (warp == 1 && lane == 0) || (warp == 4 && lane == 0)) {
+  if (threadIdx.x == 0 || (warp == 1 && lane == 0) || (warp == 2 && lane == 0) || (warp == 4 && lane == 0)) {
     if (s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   }
   tc_fence_before();
