@@ -71,6 +71,7 @@ struct Params {
   int groups;    // head groups per (layer, row)
   int items;
   int KT;        // key positions per tile: 64 packed, 128 otherwise
+  int out32;     // output base 32-byte aligned (32-byte stores)
   float scale_log2;
 };
 
@@ -107,6 +108,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 32-byte global store (8 x 32-bit), ptr 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -337,6 +345,48 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     int g = 0;
     bool alive = true;
+    // The epilogue of an item (O / l -> bf16 output row, after the item's last
+    // PV) runs, for two-head tiles, inside the next item's first tile after
+    // that tile's P is published, so the wait for the last PV overlaps the
+    // next item's first score product and softmax (the next item's first PV
+    // waits for o_free).
+    bool pend = false, pend_ok = false;
+    uint16_t* pend_row = nullptr;
+    float pend_l = 0.f;
+    int pend_g = 0;
+    auto finish = [&]() -> bool {
+      if (!warp_wait(&bars->pv_done[pend_g & 1], (pend_g >> 1) & 1, &s_abort)) return false;
+      tc_fence_after();
+      const float inv = pend_l > 0.f ? 1.f / pend_l : 0.f;
+      // O in chunks of EC columns (one TMEM wait per chunk; 128-row tiles use
+      // narrower chunks, their softmax already holds most registers).
+      constexpr int EC = PACKED ? 64 : 32;
+#pragma unroll
+      for (int h2 = 0; h2 < 128 / EC; ++h2) {
+        float o[EC];
+#pragma unroll
+        for (int q = 0; q < EC / 32; ++q) tmem_ld32(lane_addr + kColO + EC * h2 + 32 * q, o + 32 * q);
+        tmem_wait_ld();
+        if (pend_ok) {
+          uint32_t w[EC / 2];
+#pragma unroll
+          for (int e = 0; e < EC / 2; ++e) w[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
+          uint16_t* dst = pend_row + EC * h2;
+          if (p.out32) {
+#pragma unroll
+            for (int q = 0; q < EC / 16; ++q) st_global_v8(dst + 16 * q, w + 8 * q);
+          } else {
+#pragma unroll
+            for (int q = 0; q < EC / 8; ++q)
+              *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free);
+      pend = false;
+      return true;
+    };
     for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
       const Item x = decode(p, it);
       if (!x.ok) continue;
@@ -431,32 +481,24 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[pb]);
-      }
-      if (!alive) break;
-      // Epilogue: O / l -> bf16 output row, after the item's last PV.
-      if (!(alive = warp_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &s_abort))) break;
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = p.out + ((((size_t)x.lb * p.N + (row_ok ? node : 0)) * p.Hq) + (size_t)h * p.G + gq) * 128;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float o[32];
-        tmem_ld32(lane_addr + kColO + 32 * c4, o);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pk[e] = pack_bf16x2(o[q * 8 + 2 * e] * inv, o[q * 8 + 2 * e + 1] * inv);
-            *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
+        // The previous item's epilogue (its PV(0) waits for O to be read out).
+        if constexpr (PACKED) {
+          if (t == 0 && pend && !(alive = finish())) break;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);
+      if (!alive) break;
+      pend = true;
+      pend_ok = row_ok;
+      pend_row = p.out + ((((size_t)x.lb * p.N + (row_ok ? node : 0)) * p.Hq) + (size_t)h * p.G + gq) * 128;
+      pend_l = l;
+      pend_g = g - 1;
+      // 128-row tiles keep every score register live inside the tile loop:
+      // their epilogue runs here, right after the item.
+      if constexpr (!PACKED) {
+        if (!(alive = finish())) break;
+      }
     }
+    if (alive && pend) alive = finish();
   }
 
   if (threadIdx.x == 0 || (warp == 1 && lane == 0) || (warp == 2 && lane == 0) || (warp == 4 && lane == 0)) {
@@ -525,6 +567,7 @@ medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, c
   p.Lmax = Lmax;
   p.W = (N + 31) / 32;
   p.packed = N * G <= 64 ? 1 : 0;
+  p.out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.KT = p.packed ? 64 : 128;
   p.mtiles = p.packed ? 1 : (N * G + 127) / 128;
   p.groups = p.packed ? (Hkv + 1) / 2 : Hkv;
