@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kPartThreads)
 node_partial_kernel(const float* __restrict__ logits, int N, int V, int C, float T, float4* __restrict__ part) {
   __shared__ float sv[kPartThreads / 32];
   __shared__ int si[kPartThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int c = blockIdx.x, n = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const float* z = logits + ((size_t)b * N + n) * V;
   const int cs = ((V + C - 1) / C + 3) & ~3;  // chunk size, a multiple of 4
@@ -171,6 +173,8 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   __shared__ int s_key[kSelectThreads / 32];
   __shared__ int s_bad;
   const int b = blockIdx.x, tid = threadIdx.x, c = tid;
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) s_bad = 0;
   // 1. statistics of every node: grp threads per node, strided over the chunks
   {
@@ -297,10 +301,10 @@ medusa_status typical_accept_launch(const float* logits, const int32_t* tokens, 
                                     float* thr_or_null, float4* part, int32_t* d_status, cudaStream_t s) {
   const int N = t->n_nodes;
   const int C = accept_chunks(V);
-  node_partial_kernel<<<dim3(C, N, B), kPartThreads, 0, s>>>(logits, N, V, C, temperature, part);
+  launch_pdl(node_partial_kernel, dim3(C, N, B), dim3(kPartThreads), 0, s, logits, N, V, C, temperature, part);
   int grp = 1;
   while (grp < 8 && grp * 2 * N <= kSelectThreads) grp *= 2;
-  select_path_kernel<<<B, kSelectThreads, 0, s>>>(logits, tokens, t->parent, t->depth, N, V, t->max_depth, C, grp,
+  launch_pdl(select_path_kernel, dim3(B), dim3(kSelectThreads), 0, s, logits, tokens, t->parent, t->depth, N, V, t->max_depth, C, grp,
                                                   temperature, eps, delta, part, accept_len, path_nodes, next_tok,
                                                   p_tok_or_null, thr_or_null, d_status);
   return launch_status();

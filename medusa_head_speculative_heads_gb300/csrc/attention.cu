@@ -45,6 +45,8 @@ tree_attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ kc, const T
                       const uint32_t* __restrict__ mask, const int32_t* __restrict__ prefix_len,
                       int B, int N, int Hq, int Hkv, int Lmax, float scale_log2, T* __restrict__ out,
                       int32_t* d_status) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int D = 32 * DQ;
   constexpr int KP = D + 4;  // padded key row (16-byte aligned, conflict-free 128-bit reads)
   extern __shared__ __align__(16) float smem[];
@@ -180,7 +182,7 @@ static medusa_status launch_simt(const void* q, const void* kc, const void* vc, 
   const float sl2 = scale * 1.4426950408889634f;
   auto go = [&](auto kern) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, kSimtThreads, smem, s>>>((const T*)q, (const T*)kc, (const T*)vc, (const T*)kt,
+    launch_pdl(kern, dim3(grid), dim3(kSimtThreads), smem, s, (const T*)q, (const T*)kc, (const T*)vc, (const T*)kt,
                                           (const T*)vt, mask, prefix_len, B, N, Hq, Hkv, Lmax, sl2,
                                           (T*)out, d_status);
   };

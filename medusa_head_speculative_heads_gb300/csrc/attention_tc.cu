@@ -186,6 +186,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Barriers, TMEM and descriptor prefetch above touch no global memory.
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
@@ -604,7 +607,7 @@ medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, c
   const int sms = device_sm_count();
   const int rounds = (p.items + sms - 1) / sms;
   const int grid = (p.items + rounds - 1) / rounds;
-  kern<<<grid, tc::kThreads, tc::kSmemBytes, s>>>(mq, mkc, mvc, mkt, mvt, p);
+  launch_pdl(kern, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, s, mq, mkc, mvc, mkt, mvt, p);
   return launch_status();
 }
 

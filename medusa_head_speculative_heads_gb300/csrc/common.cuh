@@ -13,6 +13,16 @@ __device__ __forceinline__ void set_status(int32_t* st, int code) {
   if (st) atomicCAS(st, 0, code);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization and executes pdl_wait() before it
+// reads or writes memory that an earlier kernel on the stream may still use,
+// then pdl_trigger() so the next kernel can be scheduled while this one
+// finishes.  Because every kernel waits before completing, completion of a
+// kernel implies completion of all earlier ones.  Both are no-ops when the
+// kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // Round-to-nearest-even fp32 -> bf16 bits (inputs here are finite).

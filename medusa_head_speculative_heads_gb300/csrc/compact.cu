@@ -22,6 +22,8 @@ __global__ void kv_gather_kernel(WORD* __restrict__ kc, WORD* __restrict__ vc, c
                                  const int32_t* __restrict__ accept_len, const int32_t* __restrict__ prefix_len,
                                  int nl, int B, int N, int Lmax, int Dmax, int words_per_row,
                                  long long total, int32_t* d_status) {
+  pdl_wait();
+  pdl_trigger();
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
        t += (long long)gridDim.x * blockDim.x) {
     // t = (((l * B + b) * (Dmax+1) + i) * words_per_row + w) * 2 + kv
@@ -62,6 +64,8 @@ __global__ void kv_gather_kernel(WORD* __restrict__ kc, WORD* __restrict__ vc, c
 
 __global__ void kv_len_kernel(const int32_t* prefix_len, const int32_t* accept_len, int32_t* new_len,
                               int B, int Lmax, int Dmax, const int32_t* __restrict__ path_nodes, int N) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int L = prefix_len[b], A = accept_len[b];
@@ -106,17 +110,17 @@ extern "C" medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, c
   const long long cap = (long long)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (v16)
-    kv_gather_kernel<uint4><<<(int)blocks, threads, 0, s>>>((uint4*)kc, (uint4*)vc, (const uint4*)kt,
+    launch_pdl(kv_gather_kernel<uint4>, dim3((int)blocks), dim3(threads), 0, s, (uint4*)kc, (uint4*)vc, (const uint4*)kt,
                                                            (const uint4*)vt, path_nodes, accept_len,
                                                            prefix_len, n_layers, B, N, Lmax, Dmax,
                                                            wpr, total, d_status);
   else
-    kv_gather_kernel<uint32_t><<<(int)blocks, threads, 0, s>>>((uint32_t*)kc, (uint32_t*)vc,
+    launch_pdl(kv_gather_kernel<uint32_t>, dim3((int)blocks), dim3(threads), 0, s, (uint32_t*)kc, (uint32_t*)vc,
                                                                (const uint32_t*)kt, (const uint32_t*)vt,
                                                                path_nodes, accept_len, prefix_len,
                                                                n_layers, B, N, Lmax, Dmax, wpr, total,
                                                                d_status);
-  kv_len_kernel<<<(B + 127) / 128, 128, 0, s>>>(prefix_len, accept_len, new_len, B, Lmax, Dmax,
+  launch_pdl(kv_len_kernel, dim3((B + 127) / 128), dim3(128), 0, s, prefix_len, accept_len, new_len, B, Lmax, Dmax,
                                                 path_nodes, N);
   return launch_status();
 }

@@ -177,6 +177,8 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
                   int n_counters, float* __restrict__ top_v, int* __restrict__ top_i) {
   extern __shared__ float xs[];  // [BB][C], then [BB][cap]
   __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
   const int k = blockIdx.y;
   if constexpr (kFirst) {
     // The W2 passes that follow count their finished CTAs here.
@@ -309,6 +311,8 @@ topk_block_kernel(const float* __restrict__ x, const int* __restrict__ x_idx, in
   __shared__ int ci[kTopkChunk];
   __shared__ float sv[kTopkThreads / 32 * MEDUSA_MAX_TOPK];
   __shared__ int si[kTopkThreads / 32 * MEDUSA_MAX_TOPK];
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y, chunk = blockIdx.x, warp = threadIdx.x >> 5;
   const int lo = (int)((long long)n_per_row * chunk / chunks);
   const int hi = (int)((long long)n_per_row * (chunk + 1) / chunks);
@@ -337,10 +341,10 @@ static medusa_status launch_topk(const float* x, const int* x_idx, int rows, int
                                  int* cand_idx, float* out_val, int* out_idx, cudaStream_t s) {
   const int chunks = chunks_for(n);
   if (chunks == 1) {
-    topk_block_kernel<<<dim3(1, rows), kTopkThreads, 0, s>>>(x, x_idx, n, 1, topk, out_val, out_idx);
+    launch_pdl(topk_block_kernel, dim3(1, rows), dim3(kTopkThreads), 0, s, x, x_idx, n, 1, topk, out_val, out_idx);
   } else {
-    topk_block_kernel<<<dim3(chunks, rows), kTopkThreads, 0, s>>>(x, x_idx, n, chunks, topk, cand_val, cand_idx);
-    topk_block_kernel<<<dim3(1, rows), kTopkThreads, 0, s>>>(cand_val, cand_idx, chunks * topk, 1, topk, out_val,
+    launch_pdl(topk_block_kernel, dim3(chunks, rows), dim3(kTopkThreads), 0, s, x, x_idx, n, chunks, topk, cand_val, cand_idx);
+    launch_pdl(topk_block_kernel, dim3(1, rows), dim3(kTopkThreads), 0, s, cand_val, cand_idx, chunks * topk, 1, topk, out_val,
                                                               out_idx);
   }
   return launch_status();
@@ -388,7 +392,7 @@ static int launch_gemv_bb(int BB, const TW* W, const TW* h, const float* u, int 
     const size_t smem = xs_bytes + (kFirst ? 0 : (size_t)BB * cap * sizeof(float));
     if (smem > est) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     const bool fuse = !kFirst && top_v && merge_fits(per_head, topk, C);
-    kern<<<dim3(per_head, K), kGemvThreads, smem, s>>>(W, h, u, B, b0, K, rows_per_head, C, out, topk, cand_v,
+    launch_pdl(kern, dim3(per_head, K), dim3(kGemvThreads), smem, s, W, h, u, B, b0, K, rows_per_head, C, out, topk, cand_v,
                                                        cand_i, counters, n_counters, fuse ? top_v : nullptr,
                                                        fuse ? top_i : nullptr);
     launched = per_head;

@@ -115,6 +115,8 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = s_tmem;
   const int ksteps = p.H / 64;
   const uint32_t b_bytes = (uint32_t)p.N * 128;
@@ -299,13 +301,13 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   p.first = 1;
   p.tiles_per_head = ceil_div(H, 128);
   p.tiles = K * p.tiles_per_head;
-  kern<<<grid_for(p.tiles), htc::kThreads, smem, s>>>(ma1, mb1, p);
+  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma1, mb1, p);
   // W2: rows per head = V
   p.R = V;
   p.first = 0;
   p.tiles_per_head = ceil_div(V, 128);
   p.tiles = K * p.tiles_per_head;
-  kern<<<grid_for(p.tiles), htc::kThreads, smem, s>>>(ma2, mb2, p);
+  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma2, mb2, p);
   return launch_status();
 }
 

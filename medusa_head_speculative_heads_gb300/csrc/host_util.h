@@ -35,6 +35,25 @@ struct WsCarver {
   }
 };
 
+// Launches `kern` with programmatic stream serialization (the kernel may be
+// scheduled before the previous kernel on the stream has finished; its
+// pdl_wait() orders its memory accesses).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 inline medusa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? MEDUSA_OK : MEDUSA_ERR_CUDA;
 }

@@ -25,6 +25,8 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
                   const int32_t* __restrict__ prefix_len, int32_t* __restrict__ tokens,
                   int32_t* __restrict__ pos, uint32_t* __restrict__ mask, int32_t* d_status) {
   __shared__ int s_parent[MEDUSA_MAX_NODES], s_depth[MEDUSA_MAX_NODES];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, n = threadIdx.x;
   // Every independent load first (one round trip), then the top-k gather.
   int rk = 0, L = 0, tok0 = 0;
@@ -95,7 +97,7 @@ extern "C" medusa_status medusa_tree_build(const medusa_dev_topology* t, const i
   if (t->n_nodes < 1 || t->n_nodes > MEDUSA_MAX_NODES) return MEDUSA_ERR_INVALID_ARG;
   if (t->max_depth > K || t->max_rank > topk) return MEDUSA_ERR_INVALID_ARG;
   const int threads = (t->n_nodes + 31) / 32 * 32;
-  tree_build_kernel<<<B, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  launch_pdl(tree_build_kernel, dim3(B), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream), 
       t->parent, t->depth, t->rank, t->n_nodes, root_tok, topk_idx, K, topk, prefix_len, tokens, pos,
       mask, d_status);
   return launch_status();
