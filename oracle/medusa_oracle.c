@@ -19,7 +19,8 @@
  *    longest valid prefix kept.
  *  - same page, section "方法细节" (method details): temperature 0 reduces the
  *    typical test to greedy decoding.
- *  - same page, FAQ "树注意力为什么能一次验证多条候选": tree position encoding.
+ *  - same page, FAQ "树注意力为什么能一次验证多条候选": tree position encoding
+ *    (each node is encoded at its position in the tree).
  *  - "Medusa 多解码头推理加速全解析" (skill-pack guide), section "推理算法":
  *    per-head top-k of the head logits, candidate verification with
  *    past_key_values, "accept longest valid candidate".
@@ -342,5 +343,38 @@ int orc_kv_compact(void* kc, void* vc, const void* kt, const void* vt, int elem_
       }
     new_len[b] = L + A;
   }
+  return 0;
+}
+
+/*
+ * Rotary position embedding of the tree tokens at their tree positions.
+ * Review page, FAQ "树注意力为什么能一次验证多条候选": position encoding follows
+ * the tree, so node n of row b sits at pos[b][n] = prefix_len[b] + depth(n)
+ * (the positions medusa tree packing produces).  The pages give no formula;
+ * reading: the rotate-half rotary embedding of the LLaMA family (Vicuna is
+ * one): for i < d/2 the pair (x[i], x[i + d/2]) is rotated by the angle
+ * pos * theta_i, theta_i = base^(-2i/d):
+ *   x'[i]       = x[i] cos(a) - x[i + d/2] sin(a)
+ *   x'[i + d/2] = x[i + d/2] cos(a) + x[i] sin(a),   a = pos * theta_i.
+ * x [nl][B][N][Hx][d] (fp32 or bf16 bits) -> out (same layout) in double.
+ */
+int orc_tree_rope(const void* x, int dt, const int32_t* pos, int nl, int B, int N, int Hx, int d, double base,
+                  double* out) {
+  if (d < 2 || d % 2 || base <= 0.0) return 1;
+  const int half = d / 2;
+  for (int l = 0; l < nl; ++l)
+    for (int b = 0; b < B; ++b)
+      for (int n = 0; n < N; ++n) {
+        const double p = (double)pos[(size_t)b * N + n];
+        for (int h = 0; h < Hx; ++h) {
+          const size_t o = ((((size_t)l * B + b) * N + n) * Hx + h) * d;
+          for (int i = 0; i < half; ++i) {
+            const double a = p * pow(base, -2.0 * i / d);
+            const double x0 = orc_load(x, dt, o + i), x1 = orc_load(x, dt, o + i + half);
+            out[o + i] = x0 * cos(a) - x1 * sin(a);
+            out[o + i + half] = x1 * cos(a) + x0 * sin(a);
+          }
+        }
+      }
   return 0;
 }

@@ -49,7 +49,9 @@ def lib():
         L.orc_tree_attention.argtypes = [P, P, P, P, P, i32, P, P] + [i32] * 7 + [f64, P]
         L.orc_typical_accept.argtypes = [P, P, P, i32, i32, i32, f64, f64, f64, i32, P, P, P, P, P, P]
         L.orc_kv_compact.argtypes = [P, P, P, P, i32, P, P, P, P, P] + [i32] * 7
-        for f in (L.orc_heads, L.orc_topk_f32, L.orc_tree_attention, L.orc_typical_accept, L.orc_kv_compact):
+        L.orc_tree_rope.argtypes = [P, i32, P] + [i32] * 5 + [f64, P]
+        for f in (L.orc_heads, L.orc_topk_f32, L.orc_tree_attention, L.orc_typical_accept, L.orc_kv_compact,
+                  L.orc_tree_rope):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -159,3 +161,17 @@ def kv_compact(kc, vc, kt, vt, path_nodes, accept_len, prefix_len):
     if rc:
         raise ValueError(f"orc_kv_compact rejected its arguments ({rc})")
     return kc2, vc2, new_len, ovf.astype(bool)
+
+
+def tree_rope(x, pos, base: float = 10000.0):
+    """Rotary embedding of x [nl, B, N, Hx, d] (float32 or bf16 bits) at the tree
+    positions pos [B, N]; returns float64 of the same shape."""
+    x = np.ascontiguousarray(x)
+    nl, B, N, Hx, d = x.shape
+    pos = np.ascontiguousarray(pos, np.int32)
+    assert pos.shape == (B, N)
+    out = np.empty(x.shape, np.float64)
+    rc = lib().orc_tree_rope(_p(x), _dt(x), _p(pos), nl, B, N, Hx, d, float(base), _p(out))
+    if rc:
+        raise ValueError(f"orc_tree_rope rejected its arguments ({rc})")
+    return out

@@ -496,3 +496,75 @@ def test_kv_compact_overflow_writes_nothing():
     np.testing.assert_array_equal(kc2[:, 0], kc[:, 0])
     assert list(new_len) == [Lmax - 1, 2]
     np.testing.assert_array_equal(kc2[0, 1, 1], kt[0, 1, 2])
+
+
+# ----------------------------------------------------------------------------- tree RoPE
+
+def _rope_generator(d, base):
+    """Block skew-symmetric generator A of the rotary embedding: expm(p A)
+    turns the plane of dimensions (i, i + d/2) by p * base^(-2i/d)."""
+    A = np.zeros((d, d))
+    half = d // 2
+    for i in range(half):
+        th = base ** (-2.0 * i / d)
+        A[i + half, i] = th
+        A[i, i + half] = -th
+    return A
+
+
+def test_tree_rope_position_zero_is_identity():
+    x = _f32(np.random.default_rng(11).standard_normal((2, 1, 3, 2, 8)))
+    out = oracle.tree_rope(x, np.zeros((1, 3), np.int32))
+    np.testing.assert_array_equal(out, x.astype(np.float64))
+
+
+@pytest.mark.parametrize("d,base", [(2, 10000.0), (8, 10000.0), (64, 10000.0), (128, 500000.0)])
+def test_tree_rope_equals_matrix_exponential_of_generator(d, base):
+    """The rotation at position p is exp(p A) (scipy's matrix exponential), for
+    positions up to a long prefix plus a deep tree."""
+    from scipy.linalg import expm
+    rng = np.random.default_rng(d)
+    pos = np.array([[0, 1, 7, 1029, 4100]], np.int32)
+    x = _f32(rng.standard_normal((1, 1, pos.shape[1], 2, d)))
+    out = oracle.tree_rope(x, pos, base)
+    A = _rope_generator(d, base)
+    for n, p in enumerate(pos[0]):
+        R = expm(float(p) * A)
+        for h in range(2):
+            np.testing.assert_allclose(out[0, 0, n, h], R @ x[0, 0, n, h].astype(np.float64), rtol=0, atol=1e-9)
+
+
+def test_tree_rope_preserves_every_pair_norm():
+    rng = np.random.default_rng(3)
+    d = 16
+    x = _f32(rng.standard_normal((1, 2, 5, 3, d)))
+    pos = rng.integers(0, 5000, size=(2, 5)).astype(np.int32)
+    out = oracle.tree_rope(x, pos)
+    xd = x.astype(np.float64)
+    h = d // 2
+    np.testing.assert_allclose(out[..., :h] ** 2 + out[..., h:] ** 2, xd[..., :h] ** 2 + xd[..., h:] ** 2,
+                               rtol=1e-12)
+
+
+def test_tree_rope_scores_depend_only_on_position_difference():
+    """q at position m against k at position n gives the same dot product after
+    shifting both positions by the same amount (the property that lets tree
+    positions stand in for sequence positions)."""
+    rng = np.random.default_rng(5)
+    d = 32
+    q = _f32(rng.standard_normal((1, 1, 1, 1, d)))
+    k = _f32(rng.standard_normal((1, 1, 1, 1, d)))
+    for m, n, s in [(10, 3, 1000), (1024, 1027, 7), (5, 5, 4096)]:
+        a = np.dot(oracle.tree_rope(q, np.array([[m]], np.int32)).ravel(),
+                   oracle.tree_rope(k, np.array([[n]], np.int32)).ravel())
+        b = np.dot(oracle.tree_rope(q, np.array([[m + s]], np.int32)).ravel(),
+                   oracle.tree_rope(k, np.array([[n + s]], np.int32)).ravel())
+        assert abs(a - b) <= 1e-9 * max(1.0, abs(a))
+
+
+def test_tree_rope_reads_bf16_like_its_float_value():
+    rng = np.random.default_rng(9)
+    xf = rng.standard_normal((1, 1, 2, 2, 16)).astype(np.float32)
+    xb = wl.to_bf16_bits(xf)
+    pos = np.array([[3, 99]], np.int32)
+    np.testing.assert_array_equal(oracle.tree_rope(xb, pos), oracle.tree_rope(wl.bf16_bits_to_f32(xb), pos))
