@@ -65,7 +65,9 @@ def algorithmic_bytes(c, N):
     nl, Hq, Hkv, d, L = c["nl"], c["Hq"], c["Hkv"], c["d"], c["L"]
     attn = nl * B * (2 * L * Hkv * d + 2 * N * Hkv * d + 2 * N * Hq * d) * es + N * ((N + 31) // 32) * 4
     accept = B * N * V * 4 + B * N * 4
-    return {"heads": heads, "attention": attn, "accept": accept}
+    # tree RoPE (outside the five-call step): q and tree K read and written once, positions read
+    rope = 2 * nl * B * N * (Hq + Hkv) * d * es + B * N * 4
+    return {"heads": heads, "attention": attn, "accept": accept, "rope": rope}
 
 
 class ClockSampler:
@@ -170,7 +172,8 @@ def run_ours(args, c):
         call = {"heads": lambda: vs.heads(d["h"], d["w1"], d["w2"], stream),
                 "attention": lambda: vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"],
                                                   stream),
-                "accept": lambda: vs.accept(d["logits"], stream)}[args.profile]
+                "accept": lambda: vs.accept(d["logits"], stream),
+                "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}[args.profile]
         for _ in range(args.steps):
             call()
         torch.cuda.synchronize()
@@ -225,13 +228,30 @@ def run_ours(args, c):
     per_call = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K for j, n in enumerate(names)}
     accept_len = vs.accept_len.float().mean().item()
     assert vs.check() == 0
+    # The tree RoPE that precedes attention in a verify pass (not part of the
+    # five-call step): timed alone on copies of this workload's q and tree K.
+    # Its 33.5 MB of bf16 q / K fit in L2, so every timed call follows a write
+    # of a 256 MB buffer (L2 flushed) and is bracketed by its own events.
+    rq, rk = d["q"].clone(), d["kt"].clone()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        mg.medusa_tree_rope(rq, rk, vs.pos, stream=stream)
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        rev[i][0].record(stream)
+        mg.medusa_tree_rope(rq, rk, vs.pos, stream=stream)
+        rev[i][1].record(stream)
+    torch.cuda.synchronize()
+    per_call["rope"] = sum(a.elapsed_time(b) for a, b in rev) / K
+    del rq, rk, flush
 
     ms_per_step = elapsed_ms / K
     value = job_steps_per_s(ms_per_step, world)
     hbm, tflops, peak_src = _peaks()
     ab = algorithmic_bytes(c, N)
     rooflines = {}
-    for n in ("heads", "attention", "accept"):
+    for n in ("heads", "attention", "accept", "rope"):
         gbs = ab[n] / (per_call[n] * 1e-3) / 1e9
         rooflines[n] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                         "frac": round(gbs / hbm, 4), "algorithmic_bytes": ab[n], "us": round(per_call[n] * 1e3, 2)}
@@ -433,7 +453,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
-    ap.add_argument("--profile", choices=["heads", "attention", "accept"], default=None,
+    ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope"], default=None,
                     help="run only this call `steps` times after warm-up (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:

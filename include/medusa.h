@@ -278,6 +278,24 @@ medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, const void* 
                                 int N, int Hkv, int d, int Lmax, int Dmax, medusa_dtype dt,
                                 int32_t* d_status, medusa_stream_t stream);
 
+/* ------------------------------------------------------------- (f) tree_rope
+ * Rotary position embedding of the verify pass's tree tokens at their tree
+ * positions, in place (paper review, FAQ "树注意力为什么能一次验证多条候选":
+ * the position encoding follows the tree; pos from medusa_tree_build is
+ * prefix_len + depth).  The step just before medusa_tree_attention: q is the
+ * verify pass's query tensor and k the tree K buffer (the backbone's key
+ * projection of the tree tokens, before rotation), in the layouts of
+ * medusa_tree_attention:
+ *   q [nl][B][N][Hq][d], k [nl][B][N][Hkv][d] (or NULL: q only), pos [B][N].
+ * For i < d/2 the pair (x[i], x[i + d/2]) of every head is rotated by the
+ * angle pos[b][n] * base^(-2i/d) (the rotate-half convention of the LLaMA
+ * family; the pages give no formula, base 10000 for Vicuna).  Angles are
+ * formed and reduced in double precision, the rotation runs in fp32, values
+ * are read and written in `dt`.  d even, 2 <= d <= 256; q and k must not
+ * overlap (ALIAS).  No device-side errors. */
+medusa_status medusa_tree_rope(void* q, void* k, const int32_t* pos, int n_layers, int B, int N, int Hq,
+                               int Hkv, int d, float base, medusa_dtype dt, medusa_stream_t stream);
+
 /* ------------------------------------------------------------------ status
  * Synchronises `stream`, copies the device status word to *host_code and
  * resets it to 0.  Returns CUDA_ERROR if the stream holds a failed launch. */

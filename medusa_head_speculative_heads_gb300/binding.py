@@ -29,6 +29,7 @@ EXPORTS = (
     "medusa_tree_attention_workspace_size", "medusa_tree_attention",
     "medusa_typical_accept_workspace_size", "medusa_typical_accept", "medusa_kv_compact",
     "medusa_status_check", "medusa_status_string", "medusa_version", "medusa_typical_accept_noalloc",
+    "medusa_tree_rope",
 )
 
 
@@ -86,6 +87,7 @@ def lib():
             "medusa_typical_accept": (I, [P, P, P, I, I, F, F, F, P, P, P, P, P, P, Z, P, P]),
             "medusa_typical_accept_noalloc": (I, [P, P, P, I, I, F, F, F, P, P, P, P, P, P, P]),
             "medusa_kv_compact": (I, [P, P, P, P, P, P, P, P] + [I] * 8 + [P, P]),
+            "medusa_tree_rope": (I, [P, P, P, I, I, I, I, I, I, F, I, P]),
             "medusa_status_check": (I, [P, P, P]),
             "medusa_status_string": (ctypes.c_char_p, [I]),
             "medusa_version": (I, []),
@@ -335,6 +337,22 @@ def medusa_kv_compact(kc, vc, kt, vt, path_nodes, accept_len, prefix_len, new_le
         _ptr(kc), _ptr(vc), _ptr(kt), _ptr(vt), _ptr(path_nodes), _ptr(accept_len), _ptr(prefix_len),
         _ptr(new_len), nl, B, N, Hkv, d, Lmax, Dmax, _dtype_code(kc), _ptr(d_status), _stream(stream)))
     return new_len
+
+
+def medusa_tree_rope(q, k, pos, base: float = 10000.0, stream=None):
+    """Rotary embedding of q [nl, B, N, Hq, d] and k [nl, B, N, Hkv, d] (or None)
+    at the tree positions pos [B, N], in place; returns (q, k)."""
+    nl, B, N, Hq, d = q.shape
+    Hkv = 0
+    if k is not None:
+        if k.dtype != q.dtype or tuple(k.shape[:3]) != (nl, B, N) or k.shape[4] != d:
+            raise ValueError("k must be [nl, B, N, Hkv, d] with q's dtype, nl, B, N and d")
+        Hkv = k.shape[3]
+    if tuple(pos.shape) != (B, N):
+        raise ValueError("pos must be [B, N]")
+    _check("medusa_tree_rope", lib().medusa_tree_rope(
+        _ptr(q), _ptr(k), _ptr(pos), nl, B, N, Hq, Hkv, d, float(base), _dtype_code(q), _stream(stream)))
+    return q, k
 
 
 def medusa_status_check(d_status, stream=None) -> int:

@@ -54,6 +54,12 @@ class VerifyStep:
         B_.medusa_tree_build(self.topo, root_tok, self.topk_idx, prefix_len, self.tokens, self.pos, self.mask,
                              d_status=self.status, stream=stream)
 
+    def rope(self, q, kt, base: float = 10000.0, stream=None):
+        """Rotary embedding of the verify pass's q and tree K at this step's tree
+        positions (in place); runs between tree() and attention() when the
+        caller supplies q / K before rotation."""
+        B_.medusa_tree_rope(q, kt, self.pos, base, stream=stream)
+
     def attention(self, q, kc, vc, kt, vt, prefix_len, stream=None):
         B_.medusa_tree_attention(q, kc, vc, kt, vt, self.mask, prefix_len, out=self.attn_out, ws=self.ws_attn,
                                  d_status=self.status, stream=stream)

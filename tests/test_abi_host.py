@@ -118,4 +118,11 @@ def test_host_validation_rejects_before_launch():
     st.n_nodes = 7
     assert L.medusa_typical_accept(fake, fake, ctypes.byref(st), 1, 100, ctypes.c_float(0.5), ctypes.c_float(0.1),
                                    ctypes.c_float(0.3), fake, fake, fake, None, None, fake, 1 << 20, None, None) == 1
+    # tree_rope: odd or oversized head_dim, missing pos, q and k overlapping, bad base
+    F = ctypes.c_float
+    assert L.medusa_tree_rope(fake, P(base * 64), fake, 1, 1, 7, 4, 2, 63, F(1e4), 1, None) == 1
+    assert L.medusa_tree_rope(fake, P(base * 64), fake, 1, 1, 7, 4, 2, 512, F(1e4), 1, None) == 1
+    assert L.medusa_tree_rope(fake, P(base * 64), None, 1, 1, 7, 4, 2, 128, F(1e4), 1, None) == 1
+    assert L.medusa_tree_rope(P(base), P(base + 256), fake, 1, 1, 7, 4, 2, 128, F(1e4), 1, None) == 3
+    assert L.medusa_tree_rope(fake, None, fake, 1, 1, 7, 4, 0, 128, F(0.0), 1, None) == 1
     assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"
