@@ -186,3 +186,39 @@ def tree_build(topo: Topology, root_tok, topk_idx, prefix_len):
             mask[n, a // 32] |= np.uint32(1 << (a % 32))
             a = topo.parent[a]
     return tokens, pos, mask
+
+
+def accept_stats(topo: Topology, path_nodes, accept_len, R: int, K: int | None = None):
+    """Calibration counts from observed acceptance (paper review, "方法细节":
+    the sparse tree is built from per-head top-i accuracies measured on
+    calibration data; here they are measured on the verify steps themselves).
+
+    For every batch row, a non-root node n is *tested* when its parent lies on
+    the accepted path (its parent was accepted), and *accepted* when n itself
+    lies on the path.  Reading: "accepted" means kept on the accepted path; at
+    temperature 0 exactly the argmax-matching child is kept, so accepted /
+    tested estimates the top-(rank+1) accuracy of head depth(n).
+    Returns (tested, accepted), int64 [K][R] indexed by (depth - 1, rank).
+    """
+    K = topo.max_depth if K is None else K
+    tested = np.zeros((K, R), np.int64)
+    accepted = np.zeros((K, R), np.int64)
+    for b in range(len(accept_len)):
+        A = int(accept_len[b])
+        path = [int(x) for x in path_nodes[b][:A]]
+        for n in range(1, topo.n_nodes):
+            d = int(topo.depth[n])
+            if d - 1 < A and int(topo.parent[n]) == path[d - 1]:
+                tested[d - 1][int(topo.rank[n])] += 1
+                if d < A and path[d] == n:
+                    accepted[d - 1][int(topo.rank[n])] += 1
+    return tested, accepted
+
+
+def acc_update(acc, tested, accepted, weight: float):
+    """New accuracy table: acc'[k][i] = (accepted + weight * acc) / (tested + weight),
+    the old table counting as `weight` pseudo-observations (reading: the pages
+    measure the accuracies once; an online estimate needs a prior, and the
+    previous table is the plain one)."""
+    acc = np.asarray(acc, np.float64)
+    return (np.asarray(accepted, np.float64) + weight * acc) / (np.asarray(tested, np.float64) + weight)

@@ -568,3 +568,60 @@ def test_tree_rope_reads_bf16_like_its_float_value():
     xb = wl.to_bf16_bits(xf)
     pos = np.array([[3, 99]], np.int32)
     np.testing.assert_array_equal(oracle.tree_rope(xb, pos), oracle.tree_rope(wl.bf16_bits_to_f32(xb), pos))
+
+
+# ----------------------------------------------------------------------------- calibration statistics
+
+def test_accept_stats_worked_example_dense_2x2():
+    """Tree: 0 root, 1 = (0), 2 = (1), 3 = (0,0), 4 = (0,1), 5 = (1,0), 6 = (1,1).
+    Accepted path 0 -> 2 -> 6: at depth 1 both ranks are tested and rank 1 kept;
+    at depth 2 node 2's children (ranks 0, 1) are tested and rank 1 kept."""
+    t = topo_mod.dense([2, 2])
+    assert [tuple(p) for p in t.paths] == [(), (0,), (1,), (0, 0), (0, 1), (1, 0), (1, 1)]
+    tested, accepted = topo_mod.accept_stats(t, np.array([[0, 2, 6]], np.int32), [3], R=2)
+    np.testing.assert_array_equal(tested, [[1, 1], [1, 1]])
+    np.testing.assert_array_equal(accepted, [[0, 1], [0, 1]])
+
+
+def test_accept_stats_chain_and_root_only():
+    chain = topo_mod.dense([1] * 4)
+    tested, accepted = topo_mod.accept_stats(chain, np.arange(5, dtype=np.int32)[None], [5], R=1)
+    np.testing.assert_array_equal(tested, np.ones((4, 1)))
+    np.testing.assert_array_equal(accepted, np.ones((4, 1)))
+    t = topo_mod.dense([2, 2])
+    tested, accepted = topo_mod.accept_stats(t, np.array([[0, -1, -1]], np.int32), [1], R=2)
+    np.testing.assert_array_equal(tested, [[1, 1], [0, 0]])
+    assert accepted.sum() == 0
+
+
+def test_accept_stats_invariants_on_a_greedy_tree():
+    """Accepted counts sum to accept_len - 1 per row; at every depth d <= accept_len
+    the tested count is the number of children of the accepted node at depth d - 1."""
+    t = topo_mod.greedy(topo_mod.synthetic_accuracy(4, 10), 64)
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        # random root-to-node path of random length
+        n = int(rng.integers(0, t.n_nodes))
+        path = []
+        while n >= 0:
+            path.append(n)
+            n = int(t.parent[n])
+        path = path[::-1]
+        A = len(path)
+        pn = np.full((1, t.max_depth + 1), -1, np.int32)
+        pn[0, :A] = path
+        tested, accepted = topo_mod.accept_stats(t, pn, [A], R=10)
+        assert accepted.sum() == A - 1
+        for d in range(1, t.max_depth + 1):
+            want = len(t.children(path[d - 1])) if d - 1 < A else 0
+            assert tested[d - 1].sum() == want
+
+
+def test_acc_update_limits():
+    acc = np.array([[0.5, 0.25]])
+    tested = np.array([[10, 0]])
+    accepted = np.array([[7, 0]])
+    np.testing.assert_array_equal(topo_mod.acc_update(acc, tested, accepted, 0.0)[0, 0], 0.7)
+    out = topo_mod.acc_update(acc, tested, accepted, 5.0)
+    assert out[0, 0] == (7 + 2.5) / 15 and out[0, 1] == 0.25  # an untested rank keeps its value
+    np.testing.assert_allclose(topo_mod.acc_update(acc, tested, accepted, 1e12), acc, rtol=1e-10)
