@@ -219,6 +219,10 @@ def acc_update(acc, tested, accepted, weight: float):
     """New accuracy table: acc'[k][i] = (accepted + weight * acc) / (tested + weight),
     the old table counting as `weight` pseudo-observations (reading: the pages
     measure the accuracies once; an online estimate needs a prior, and the
-    previous table is the plain one)."""
+    previous table is the plain one).  An entry with tested + weight == 0 keeps
+    its value."""
     acc = np.asarray(acc, np.float64)
-    return (np.asarray(accepted, np.float64) + weight * acc) / (np.asarray(tested, np.float64) + weight)
+    den = np.asarray(tested, np.float64) + weight
+    with np.errstate(invalid="ignore", divide="ignore"):
+        new = (np.asarray(accepted, np.float64) + weight * acc) / den
+    return np.where(den > 0, new, acc)  # nothing observed and no prior weight: unchanged

@@ -621,7 +621,7 @@ def test_acc_update_limits():
     acc = np.array([[0.5, 0.25]])
     tested = np.array([[10, 0]])
     accepted = np.array([[7, 0]])
-    np.testing.assert_array_equal(topo_mod.acc_update(acc, tested, accepted, 0.0)[0, 0], 0.7)
+    np.testing.assert_array_equal(topo_mod.acc_update(acc, tested, accepted, 0.0), [[0.7, 0.25]])
     out = topo_mod.acc_update(acc, tested, accepted, 5.0)
     assert out[0, 0] == (7 + 2.5) / 15 and out[0, 1] == 0.25  # an untested rank keeps its value
     np.testing.assert_allclose(topo_mod.acc_update(acc, tested, accepted, 1e12), acc, rtol=1e-10)
