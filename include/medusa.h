@@ -296,6 +296,48 @@ medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, const void* 
 medusa_status medusa_tree_rope(void* q, void* k, const int32_t* pos, int n_layers, int B, int N, int Hq,
                                int Hkv, int d, float base, medusa_dtype dt, medusa_stream_t stream);
 
+/* ------------------------------------------------ (f3) online tree calibration
+ * The sparse tree of the paper review ("方法细节") is built from per-head top-i
+ * accuracies measured on calibration data; these calls measure them on the
+ * verify steps and rebuild the tree on the device.
+ *
+ * medusa_accept_stats: adds this step's observations to the counts.  For every
+ * batch row, a non-root node n is tested when its parent is on the accepted
+ * path and accepted when n is on it (reading: kept on the path; at
+ * temperature 0 exactly the argmax-matching child is kept).
+ *   path_nodes [B][Dmax+1], accept_len [B] from medusa_typical_accept;
+ *   tested, accepted [Dmax][R] uint64, row = depth - 1, column = rank
+ *   (caller-owned, zeroed by the caller; atomically incremented).
+ *   Dmax >= t->max_depth, t->max_rank <= R <= MEDUSA_MAX_TOPK.
+ *   accept_len outside 1..Dmax+1 sets BAD_INDEX (row skipped). */
+medusa_status medusa_accept_stats(const int32_t* path_nodes, const int32_t* accept_len,
+                                  const medusa_dev_topology* t, int B, int Dmax, int R, uint64_t* tested,
+                                  uint64_t* accepted, int32_t* d_status, medusa_stream_t stream);
+
+/* medusa_acc_update: acc[k][i] = (accepted + weight * acc) / (tested + weight)
+ * in place on the device table acc [K][R] (fp64), the old table counting as
+ * `weight` pseudo-observations; an entry with tested + weight == 0 keeps its
+ * value.  Each operation is rounded on its own (IEEE double).  weight >= 0. */
+medusa_status medusa_acc_update(double* acc, const uint64_t* tested, const uint64_t* accepted, int K, int R,
+                                double weight, medusa_stream_t stream);
+
+/* medusa_topology_greedy_device: the greedy sparse tree of
+ * medusa_topology_greedy (same gains, ties and canonical order) built from the
+ * device table acc [K][R] (fp64, entries in [0, 1]; others are clamped and set
+ * BAD_INDEX) by one CTA, written to the caller's device buffer d_buf
+ * (>= medusa_topology_greedy_device_elems(K, n_nodes) int32):
+ *   parent[n_nodes], depth[n_nodes], rank[n_nodes], retrieve[n_nodes][K+1].
+ * `out` receives pointers into d_buf with n_nodes exact and the bounds
+ * max_depth = K, max_rank = R, n_leaves = n_nodes (retrieve rows past the real
+ * leaf count are -1); the exact {n_nodes, max_depth, n_leaves, max_rank} are
+ * written to d_meta[4].  Enqueued on `stream` like any other call, so later
+ * calls on the stream see the new tree.  INVALID_ARG unless
+ * 1 + R + ... + R^K >= n_nodes (the tree can always be completed). */
+size_t medusa_topology_greedy_device_elems(int K, int n_nodes);
+medusa_status medusa_topology_greedy_device(const double* acc, int K, int R, int n_nodes, int32_t* d_buf,
+                                            size_t buf_elems, int32_t* d_meta, medusa_dev_topology* out,
+                                            int32_t* d_status, medusa_stream_t stream);
+
 /* ------------------------------------------------------------------ status
  * Synchronises `stream`, copies the device status word to *host_code and
  * resets it to 0.  Returns CUDA_ERROR if the stream holds a failed launch. */

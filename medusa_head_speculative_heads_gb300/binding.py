@@ -29,7 +29,8 @@ EXPORTS = (
     "medusa_tree_attention_workspace_size", "medusa_tree_attention",
     "medusa_typical_accept_workspace_size", "medusa_typical_accept", "medusa_kv_compact",
     "medusa_status_check", "medusa_status_string", "medusa_version", "medusa_typical_accept_noalloc",
-    "medusa_tree_rope",
+    "medusa_tree_rope", "medusa_accept_stats", "medusa_acc_update", "medusa_topology_greedy_device_elems",
+    "medusa_topology_greedy_device",
 )
 
 
@@ -88,6 +89,10 @@ def lib():
             "medusa_typical_accept_noalloc": (I, [P, P, P, I, I, F, F, F, P, P, P, P, P, P, P]),
             "medusa_kv_compact": (I, [P, P, P, P, P, P, P, P] + [I] * 8 + [P, P]),
             "medusa_tree_rope": (I, [P, P, P, I, I, I, I, I, I, F, I, P]),
+            "medusa_accept_stats": (I, [P, P, P, I, I, I, P, P, P, P]),
+            "medusa_acc_update": (I, [P, P, P, I, I, ctypes.c_double, P]),
+            "medusa_topology_greedy_device_elems": (Z, [I, I]),
+            "medusa_topology_greedy_device": (I, [P, I, I, I, P, Z, P, P, P, P]),
             "medusa_status_check": (I, [P, P, P]),
             "medusa_status_string": (ctypes.c_char_p, [I]),
             "medusa_version": (I, []),
@@ -353,6 +358,41 @@ def medusa_tree_rope(q, k, pos, base: float = 10000.0, stream=None):
     _check("medusa_tree_rope", lib().medusa_tree_rope(
         _ptr(q), _ptr(k), _ptr(pos), nl, B, N, Hq, Hkv, d, float(base), _dtype_code(q), _stream(stream)))
     return q, k
+
+
+def medusa_accept_stats(path_nodes, accept_len, topo: DevTopology, R: int, tested, accepted, d_status=None,
+                        stream=None):
+    """Adds the step's acceptance observations to tested / accepted (int64 [Dmax][R],
+    Dmax = path_nodes.shape[1] - 1); returns (tested, accepted)."""
+    B, D1 = path_nodes.shape
+    if tuple(tested.shape) != (D1 - 1, R) or tuple(accepted.shape) != (D1 - 1, R):
+        raise ValueError("tested / accepted must be [Dmax, R]")
+    _check("medusa_accept_stats", lib().medusa_accept_stats(
+        _ptr(path_nodes), _ptr(accept_len), ctypes.byref(topo.st), B, D1 - 1, R, _ptr(tested), _ptr(accepted),
+        _ptr(d_status), _stream(stream)))
+    return tested, accepted
+
+
+def medusa_acc_update(acc, tested, accepted, weight: float, stream=None):
+    """In place on the fp64 table acc [K, R] (tested / accepted: the first K rows are used)."""
+    K, R = acc.shape
+    _check("medusa_acc_update", lib().medusa_acc_update(
+        _ptr(acc), _ptr(tested), _ptr(accepted), K, R, float(weight), _stream(stream)))
+    return acc
+
+
+def medusa_topology_greedy_device(acc, n_nodes: int, d_status=None, stream=None):
+    """Greedy sparse tree from the device fp64 table acc [K, R]; returns
+    (DevTopology, meta) with meta = int32 [4] {n_nodes, max_depth, n_leaves, max_rank}."""
+    import torch
+    K, R = acc.shape
+    elems = lib().medusa_topology_greedy_device_elems(K, n_nodes)
+    buf = torch.empty(max(1, elems), dtype=torch.int32, device=acc.device)
+    meta = torch.empty(4, dtype=torch.int32, device=acc.device)
+    st = medusa_dev_topology()
+    _check("medusa_topology_greedy_device", lib().medusa_topology_greedy_device(
+        _ptr(acc), K, R, n_nodes, _ptr(buf), elems, _ptr(meta), ctypes.byref(st), _ptr(d_status), _stream(stream)))
+    return DevTopology(st, (buf, meta)), meta
 
 
 def medusa_status_check(d_status, stream=None) -> int:

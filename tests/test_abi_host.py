@@ -125,4 +125,19 @@ def test_host_validation_rejects_before_launch():
     assert L.medusa_tree_rope(fake, P(base * 64), None, 1, 1, 7, 4, 2, 128, F(1e4), 1, None) == 1
     assert L.medusa_tree_rope(P(base), P(base + 256), fake, 1, 1, 7, 4, 2, 128, F(1e4), 1, None) == 3
     assert L.medusa_tree_rope(fake, None, fake, 1, 1, 7, 4, 0, 128, F(0.0), 1, None) == 1
+    # calibration: a tree that cannot be completed, R below the tree's ranks, a negative weight
+    meta_out = binding.medusa_dev_topology()
+    assert L.medusa_topology_greedy_device(fake, 1, 3, 5, fake, 1 << 20, fake, ctypes.byref(meta_out), None,
+                                           None) == 1
+    assert L.medusa_topology_greedy_device(fake, 2, 3, 14, fake, 1 << 20, fake, ctypes.byref(meta_out), None,
+                                           None) == 1  # 1 + 3 + 9 = 13 < 14 nodes exist
+    assert L.medusa_topology_greedy_device(fake, 2, 3, 13, fake, 10, fake, ctypes.byref(meta_out), None,
+                                           None) == 1  # buffer too small
+    assert L.medusa_topology_greedy_device_elems(4, 64) == 3 * 64 + 64 * 5
+    st2 = binding.medusa_dev_topology()
+    st2.n_nodes, st2.max_depth, st2.max_rank = 7, 2, 4
+    st2.parent = st2.depth = st2.rank = 4096
+    assert L.medusa_accept_stats(fake, fake, ctypes.byref(st2), 1, 2, 3, fake, fake, None, None) == 1
+    assert L.medusa_accept_stats(fake, fake, ctypes.byref(st2), 1, 1, 4, fake, fake, None, None) == 1
+    assert L.medusa_acc_update(fake, fake, fake, 2, 3, -1.0, None) == 1
     assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"
