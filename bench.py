@@ -124,7 +124,6 @@ def run_ours(args, c):
     import medusa_head_speculative_heads_gb300 as mg
     from medusa_head_speculative_heads_gb300.build import build as build_lib
     from medusa_head_speculative_heads_gb300.step import VerifyStep
-    from oracle import topology as otopo
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -139,7 +138,7 @@ def run_ours(args, c):
         dist.barrier()
     mg.lib()
 
-    topo = mg.Topology.greedy(np.array(otopo.synthetic_accuracy(c["K"], c["tree"][1])), c["tree"][2])
+    topo = mg.Topology.greedy(np.array(wl.synthetic_accuracy(c["K"], c["tree"][1])), c["tree"][2])
     N = topo.n_nodes
     inp = make_inputs(c, N)
     tdev = lambda a: _to_dev(a, dev)  # noqa: E731
@@ -245,6 +244,7 @@ def run_ours(args, c):
     torch.cuda.synchronize()
     per_call["rope"] = sum(a.elapsed_time(b) for a, b in rev) / K
     del rq, rk, flush
+    calib = time_calibration(mg, vs, c, N, K, stream, dev)
 
     ms_per_step = elapsed_ms / K
     value = job_steps_per_s(ms_per_step, world)
@@ -271,11 +271,42 @@ def run_ours(args, c):
                 "config": config_json(c, N),
                 "accepted_tok_per_s": round(value * c["B"] * accept_len, 2), "mean_accept_len": accept_len,
                 "per_call_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
-                "roofline": roof, "rooflines": rooflines, "e2e": e2e, "cpu_baseline": cpu,
+                "roofline": roof, "rooflines": rooflines, "calibration": calib, "e2e": e2e, "cpu_baseline": cpu,
                 "gpu_launches": K * vs.launches_per_step(), "clocks": clocks}
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_calibration(mg, vs, c, N, K, stream, dev):
+    """Online tree calibration calls (outside the five-call step): this step's
+    acceptance statistics, the accuracy-table update and a device rebuild of the
+    greedy tree, each timed with CUDA events over K calls."""
+    import torch
+    R = c["topk"]
+    Dmax = vs.path_nodes.shape[1] - 1
+    tested = torch.zeros((Dmax, R), dtype=torch.int64, device=dev)
+    accepted = torch.zeros_like(tested)
+    acc = torch.tensor(wl.synthetic_accuracy(c["K"], c["tree"][1]), dtype=torch.float64, device=dev)
+    calls = {
+        "accept_stats": lambda: mg.medusa_accept_stats(vs.path_nodes, vs.accept_len, vs.topo, R, tested, accepted,
+                                                       stream=stream),
+        "acc_update": lambda: mg.medusa_acc_update(acc[:Dmax], tested, accepted, 64.0, stream=stream),
+        "greedy_rebuild": lambda: mg.medusa_topology_greedy_device(acc, N, stream=stream),
+    }
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name + "_us"] = round(e0.elapsed_time(e1) / K * 1e3, 2)
+    out["tree"] = f"{N} nodes from a {c['K']} x {c['tree'][1]} accuracy table"
+    return out
 
 
 def max_over_ranks(elapsed_ms: float, world: int, device) -> float:

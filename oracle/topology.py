@@ -155,9 +155,9 @@ def greedy(acc, n_nodes: int, order_out: list | None = None) -> Topology:
     return Topology(canonical(chosen))
 
 
-def synthetic_accuracy(K: int = 4, R: int = 10) -> list:
-    """Per-head top-i accuracy table acc[k][i] = 0.6 * 0.8^k * 0.7^i (k, i 0-based)."""
-    return [[0.6 * 0.8 ** k * 0.7 ** i for i in range(R)] for k in range(K)]
+# The synthetic accuracy table is workload data, shared with the benchmark from
+# the input-generator module.
+from workloads import synthetic_accuracy  # noqa: E402,F401
 
 
 def tree_build(topo: Topology, root_tok, topk_idx, prefix_len):

@@ -82,6 +82,12 @@ def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
+def synthetic_accuracy(K: int = 4, R: int = 10) -> list:
+    """Per-head top-i accuracy table acc[k][i] = 0.6 * 0.8^k * 0.7^i (k, i 0-based),
+    the stand-in for the calibration accuracies the sparse tree is built from."""
+    return [[0.6 * 0.8 ** k * 0.7 ** i for i in range(R)] for k in range(K)]
+
+
 def hidden(c: dict, rows=None) -> np.ndarray:
     rows = range(c["B"]) if rows is None else rows
     return np.stack([_normal(rng(c["cfg_id"], T_H, 0, b), (c["H"],), 1.0, c["dtype"]) for b in rows])
