@@ -175,3 +175,15 @@ def tree_rope(x, pos, base: float = 10000.0):
     if rc:
         raise ValueError(f"orc_tree_rope rejected its arguments ({rc})")
     return out
+
+
+def linear(x, w):
+    """One linear layer of the verify pass over the tree tokens: y = x W^T in
+    float64 (x [T, K], w [Nout, K], float32 or bf16 bits).  The definition with
+    numpy's matrix product as the only step."""
+    def f64(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        return a.astype(np.float64)
+    return f64(x) @ f64(w).T

@@ -625,3 +625,31 @@ def test_acc_update_limits():
     out = topo_mod.acc_update(acc, tested, accepted, 5.0)
     assert out[0, 0] == (7 + 2.5) / 15 and out[0, 1] == 0.25  # an untested rank keeps its value
     np.testing.assert_allclose(topo_mod.acc_update(acc, tested, accepted, 1e12), acc, rtol=1e-10)
+
+
+# ----------------------------------------------------------------------------- verify-pass linear layer
+
+def test_linear_matches_brute_force_loops():
+    rng = np.random.default_rng(13)
+    for T, K, N in [(1, 1, 1), (3, 5, 2), (4, 8, 7)]:
+        x = _f32(rng.standard_normal((T, K)))
+        w = _f32(rng.standard_normal((N, K)))
+        y = oracle.linear(x, w)
+        for t in range(T):
+            for n in range(N):
+                ref = math.fsum(float(x[t, k]) * float(w[n, k]) for k in range(K))
+                assert abs(y[t, n] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def test_linear_identity_weight_and_rank_one_closed_form():
+    rng = np.random.default_rng(14)
+    x = wl.to_bf16_bits(rng.standard_normal((6, 16)).astype(np.float32))
+    eye = wl.to_bf16_bits(np.eye(16, dtype=np.float32))
+    np.testing.assert_array_equal(oracle.linear(x, eye), wl.bf16_bits_to_f32(x).astype(np.float64))
+    a = _f32(rng.standard_normal(5))
+    b = _f32(rng.standard_normal(9))
+    x1 = _f32(rng.standard_normal((3, 9)))
+    w1 = _f32(np.outer(a, b))  # y[t][n] = a[n] (b . x[t])
+    y = oracle.linear(x1, w1)
+    want = np.outer(x1.astype(np.float64) @ b.astype(np.float64), a.astype(np.float64))
+    np.testing.assert_allclose(y, want, rtol=1e-6)
