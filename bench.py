@@ -230,7 +230,8 @@ def run_ours(args, c):
     # The tree RoPE that precedes attention in a verify pass (not part of the
     # five-call step): timed alone on copies of this workload's q and tree K.
     # Its 33.5 MB of bf16 q / K fit in L2, so every timed call follows a write
-    # of a 256 MB buffer (L2 flushed) and is bracketed by its own events.
+    # of a 256 MB buffer (L2 flushed) and a short GPU sleep (so the host's
+    # enqueue of the call is not inside the events), and has its own events.
     rq, rk = d["q"].clone(), d["kt"].clone()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(3):
@@ -238,6 +239,7 @@ def run_ours(args, c):
     rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         flush.fill_(i & 0xff)
+        torch.cuda._sleep(200000)  # ~0.1 ms of GPU time: the host enqueues the call before the start event fires
         rev[i][0].record(stream)
         mg.medusa_tree_rope(rq, rk, vs.pos, stream=stream)
         rev[i][1].record(stream)
@@ -245,6 +247,7 @@ def run_ours(args, c):
     per_call["rope"] = sum(a.elapsed_time(b) for a, b in rev) / K
     del rq, rk, flush
     calib = time_calibration(mg, vs, c, N, K, stream, dev)
+    linear = time_linear(mg, c, stream, dev, min(K, 50))
 
     ms_per_step = elapsed_ms / K
     value = job_steps_per_s(ms_per_step, world)
@@ -271,7 +274,8 @@ def run_ours(args, c):
                 "config": config_json(c, N),
                 "accepted_tok_per_s": round(value * c["B"] * accept_len, 2), "mean_accept_len": accept_len,
                 "per_call_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
-                "roofline": roof, "rooflines": rooflines, "calibration": calib, "e2e": e2e, "cpu_baseline": cpu,
+                "roofline": roof, "rooflines": rooflines, "calibration": calib, "linear": linear, "e2e": e2e,
+                "cpu_baseline": cpu,
                 "gpu_launches": K * vs.launches_per_step(), "clocks": clocks}
         print(json.dumps(line))
     if world > 1:
@@ -306,6 +310,43 @@ def time_calibration(mg, vs, c, N, K, stream, dev):
         torch.cuda.synchronize()
         out[name + "_us"] = round(e0.elapsed_time(e1) / K * 1e3, 2)
     out["tree"] = f"{N} nodes from a {c['K']} x {c['tree'][1]} accuracy table"
+    return out
+
+
+def time_linear(mg, c, stream, dev, reps):
+    """The verify pass's linear layer (outside the five-call step) at the 7B
+    hidden size, H x H weight, over 64 to 4096 tree tokens (B * N for B = 1 to
+    64 at 64 nodes).  The weight fits in L2, so every call follows a 256 MB
+    write (L2 flushed) and has its own events."""
+    import torch
+    H = c["H"]
+    hbm, tflops, _ = _peaks()
+    g = torch.Generator(device=dev).manual_seed(0)
+    w = (torch.randn((H, H), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {"weight": f"{H} x {H} bf16", "peak_tflops": tflops, "peak_gbs": hbm}
+    for T in (64, 256, 1024, 4096):
+        x = torch.randn((T, H), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = mg.lib().medusa_linear_workspace_size(T, H, H)
+        wsb = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            mg.medusa_linear(x, w, y, ws=wsb, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i in range(reps):
+            flush.fill_(i & 0xff)
+            torch.cuda._sleep(200000)  # the host's enqueue of the call is not timed
+            ev[i][0].record(stream)
+            mg.medusa_linear(x, w, y, ws=wsb, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        us = sum(a.elapsed_time(b) for a, b in ev) / reps * 1e3
+        flops = 2.0 * T * H * H
+        byts = 2.0 * (H * H + 2 * T * H)
+        out[f"T{T}"] = {"us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+                        "tensor_frac": round(flops / us / 1e6 / tflops, 4),
+                        "gbs": round(byts / us / 1e3, 1), "hbm_frac": round(byts / us / 1e3 / hbm, 4)}
+    del flush
     return out
 
 

@@ -296,6 +296,23 @@ medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, const void* 
 medusa_status medusa_tree_rope(void* q, void* k, const int32_t* pos, int n_layers, int B, int N, int Hq,
                                int Hkv, int d, float base, medusa_dtype dt, medusa_stream_t stream);
 
+/* --------------------------------------------------------------- (f2) linear
+ * One linear layer of the verify pass over the tree tokens (paper review,
+ * roofline in "实验设计与结果" and "局限性": verifying N candidates runs every
+ * linear layer of the backbone over B * N tokens, which lifts decoding's
+ * operational intensity; past a batch of about 32 these layers turn
+ * compute-bound): y = x W^T on tcgen05 tensor cores.
+ *   x [T][K] (T = B * N tokens), W [Nout][K] (row-major (out, in)), y [T][Nout];
+ *   bf16 only (UNSUPPORTED otherwise), fp32 accumulation, y rounded once to
+ *   bf16.  K % 8 == 0, pointers 16-byte aligned; y must not overlap x or W
+ *   (ALIAS).  When the output tiles are too few to occupy the GPU, the K range
+ *   is split and the partials are added in a fixed order (deterministic);
+ *   the scratch for that is medusa_linear_workspace_size(T, K, Nout) bytes
+ *   (for the current device; 0 = none needed), 16-byte aligned. */
+size_t medusa_linear_workspace_size(int T, int K, int Nout);
+medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
+                            void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
+
 /* ------------------------------------------------ (f3) online tree calibration
  * The sparse tree of the paper review ("方法细节") is built from per-head top-i
  * accuracies measured on calibration data; these calls measure them on the

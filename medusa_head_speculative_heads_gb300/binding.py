@@ -30,7 +30,7 @@ EXPORTS = (
     "medusa_typical_accept_workspace_size", "medusa_typical_accept", "medusa_kv_compact",
     "medusa_status_check", "medusa_status_string", "medusa_version", "medusa_typical_accept_noalloc",
     "medusa_tree_rope", "medusa_accept_stats", "medusa_acc_update", "medusa_topology_greedy_device_elems",
-    "medusa_topology_greedy_device",
+    "medusa_topology_greedy_device", "medusa_linear_workspace_size", "medusa_linear",
 )
 
 
@@ -90,6 +90,8 @@ def lib():
             "medusa_kv_compact": (I, [P, P, P, P, P, P, P, P] + [I] * 8 + [P, P]),
             "medusa_tree_rope": (I, [P, P, P, I, I, I, I, I, I, F, I, P]),
             "medusa_accept_stats": (I, [P, P, P, I, I, I, P, P, P, P]),
+            "medusa_linear_workspace_size": (Z, [I, I, I]),
+            "medusa_linear": (I, [P, P, P, I, I, I, I, P, Z, P, P]),
             "medusa_acc_update": (I, [P, P, P, I, I, ctypes.c_double, P]),
             "medusa_topology_greedy_device_elems": (Z, [I, I]),
             "medusa_topology_greedy_device": (I, [P, I, I, I, P, Z, P, P, P, P]),
@@ -358,6 +360,22 @@ def medusa_tree_rope(q, k, pos, base: float = 10000.0, stream=None):
     _check("medusa_tree_rope", lib().medusa_tree_rope(
         _ptr(q), _ptr(k), _ptr(pos), nl, B, N, Hq, Hkv, d, float(base), _dtype_code(q), _stream(stream)))
     return q, k
+
+
+def medusa_linear(x, w, y=None, ws=None, d_status=None, stream=None):
+    """y [T, Nout] = x [T, K] @ w [Nout, K]^T (bf16, fp32 accumulation)."""
+    import torch
+    T, K = x.shape
+    Nout = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("w must be [Nout, K]")
+    if y is None:
+        y = torch.empty((T, Nout), dtype=x.dtype, device=x.device)
+    ws = _ws(lib().medusa_linear_workspace_size(T, K, Nout), x.device, ws)
+    _check("medusa_linear", lib().medusa_linear(
+        _ptr(x), _ptr(w), _ptr(y), T, K, Nout, _dtype_code(x), _ptr(ws), 0 if ws is None else ws.numel(),
+        _ptr(d_status), _stream(stream)))
+    return y
 
 
 def medusa_accept_stats(path_nodes, accept_len, topo: DevTopology, R: int, tested, accepted, d_status=None,

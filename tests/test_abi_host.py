@@ -140,4 +140,11 @@ def test_host_validation_rejects_before_launch():
     assert L.medusa_accept_stats(fake, fake, ctypes.byref(st2), 1, 2, 3, fake, fake, None, None) == 1
     assert L.medusa_accept_stats(fake, fake, ctypes.byref(st2), 1, 1, 4, fake, fake, None, None) == 1
     assert L.medusa_acc_update(fake, fake, fake, 2, 3, -1.0, None) == 1
+    # linear: K not a multiple of 8, fp32, y inside x, workspace too small
+    assert L.medusa_linear(fake, fake, P(base * 64), 64, 100, 128, 1, None, 0, None, None) == 1
+    assert L.medusa_linear(fake, fake, P(base * 64), 64, 128, 128, 0, None, 0, None, None) == 2
+    assert L.medusa_linear(P(base), P(base * 64), P(base + 256), 64, 128, 128, 1, None, 0, None, None) == 3
+    if L.medusa_linear_workspace_size(64, 4096, 4096):
+        assert L.medusa_linear(P(base), P(base * 64), P(base * 128), 64, 4096, 4096, 1, P(base * 256), 16, None,
+                               None) == 5
     assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"
