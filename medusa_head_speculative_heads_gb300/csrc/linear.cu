@@ -11,14 +11,13 @@
 //
 // Tiles of 128 output features (the weight rows, MMA M = 128) by up to 256
 // tokens (MMA N = TN).  Few tiles (small T, narrow layers) would leave SMs idle
-// while the weights stream from HBM, so each tile's K range is split S ways;
-// the last unit to finish a tile adds the S fp32 partials in a fixed order and
-// writes y (deterministic).  Roles (256 threads, persistent over the units):
+// while the weights stream from HBM, so each tile's K range is split S ways
+// into fp32 partials, which a second kernel adds in a fixed order (one thread
+// per output element, every SM busy; deterministic).  Roles (256 threads, persistent over the units):
 // warp 0 lane 0 issues TMA loads of the W and x boxes (128-byte swizzle) into a
 // 4- to 8-stage ring; warp 1 owns TMEM and lane 0 issues the MMAs into one of
 // two 256-column accumulators; warps 4-7 read the accumulator 32 columns at a
-// time (one feature row per thread) and write y or the partial; with split K
-// each epilogue warp counts its own finished units per tile.  Every wait is
+// time (one feature row per thread) and write y or the partial.  Every wait is
 // bounded; a timeout sets MEDUSA_DEV_TIMEOUT, drains and frees TMEM.
 #include <cuda.h>
 #include <math.h>
@@ -46,8 +45,7 @@ struct Params {
   int T, K, Nout, TN, mtiles, ntiles, S, kblocks, units, stages;
   uint32_t stage_bytes;
   uint16_t* y;
-  float* part;       // [tiles][S][128][TN] when S > 1
-  int* counters;     // [tiles][4] (per epilogue warp), zero on entry, left zero
+  float* part;       // [tiles][S][TN][128] when S > 1 (feature fastest: coalesced)
   int32_t* d_status;
 };
 
@@ -184,7 +182,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       const int n = x.mt * 128 + m;      // output feature of this thread
       const int t0 = x.nt * p.TN;        // first token of the tile
       const bool direct = p.S == 1;
-      float* prow = direct ? nullptr : p.part + (((size_t)x.tile * p.S + x.s) * 128 + m) * p.TN;
+      float* pbase = direct ? nullptr : p.part + ((size_t)x.tile * p.S + x.s) * p.TN * 128 + m;
       for (int c = 0; c < p.TN; c += 32) {
         float v[32];
         tmem_ld32(lane_addr + ab * 256 + c, v);
@@ -199,44 +197,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)  // TN is a multiple of 16: the last chunk may be half used
-            if (c + j < p.TN) *reinterpret_cast<float4*>(prow + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          for (int j = 0; j < 32; ++j)  // TN is a multiple of 16: the last chunk may be half used
+            if (c + j < p.TN) pbase[(size_t)(c + j) * 128] = v[j];
         }
       }
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[ab]);
-      if (direct) continue;
-      // Split K: per epilogue warp (its 32 feature rows), the last unit of the
-      // tile adds the partials in s order.  No barrier across warps, so a
-      // warp that stops on a timeout cannot strand the others.
-      __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(&p.counters[x.tile * 4 + (warp - 4)], 1) == p.S - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        const float* base = p.part + ((size_t)x.tile * p.S * 128 + m) * p.TN;
-        for (int c = 0; c < p.TN; c += 4) {
-          float4 acc = __ldcg(reinterpret_cast<const float4*>(base + c));
-          for (int s = 1; s < p.S; ++s) {
-            const float4 q = __ldcg(reinterpret_cast<const float4*>(base + (size_t)s * 128 * p.TN + c));
-            acc.x += q.x;
-            acc.y += q.y;
-            acc.z += q.z;
-            acc.w += q.w;
-          }
-          const float r[4] = {acc.x, acc.y, acc.z, acc.w};
-          if (n < p.Nout) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int t = t0 + c + j;
-              if (t < p.T) p.y[(size_t)t * p.Nout + n] = (uint16_t)f32_to_bf16_bits(r[j]);
-            }
-          }
-        }
-        if (lane == 0) p.counters[x.tile * 4 + (warp - 4)] = 0;  // ready for the next call
-      }
     }
   }
 
@@ -245,6 +211,23 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Split K: y[t][n] = bf16(sum over s of the partials), s in order.  One thread
+// per output element, feature fastest (coalesced partial reads and y writes).
+__global__ void __launch_bounds__(256)
+linear_reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, int T, int Nout, int TN,
+                     int mtiles, int S) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)T * Nout) return;
+  const int t = (int)(i / Nout), n = (int)(i - (size_t)t * Nout);
+  const int tile = (t / TN) * mtiles + n / 128, col = t % TN, row = n % 128;
+  const float* src = part + (((size_t)tile * S) * TN + col) * 128 + row;
+  float acc = 0.f;
+  for (int s = 0; s < S; ++s) acc += __ldcg(src + (size_t)s * TN * 128);
+  y[i] = (uint16_t)f32_to_bf16_bits(acc);
 }
 
 // ------------------------------------------------------------------ host side
@@ -279,7 +262,7 @@ static bool linear_map(CUtensorMap* m, const void* base, int cols, long long row
 struct LinearPlan {
   int TN, mtiles, ntiles, S, kblocks, units, grid, stages;
   uint32_t stage_bytes;
-  size_t part_bytes, counter_bytes;
+  size_t part_bytes;
 };
 
 static LinearPlan linear_plan(int T, int K, int Nout) {
@@ -316,7 +299,7 @@ static LinearPlan linear_plan(int T, int K, int Nout) {
   L.stages = (int)(lin::kRingBytes / L.stage_bytes);
   if (L.stages > lin::kMaxStages) L.stages = lin::kMaxStages;
   L.part_bytes = L.S > 1 ? (size_t)tiles * L.S * 128 * L.TN * sizeof(float) : 0;
-  L.counter_bytes = L.S > 1 ? (size_t)tiles * 4 * sizeof(int) : 0;
+
   return L;
 }
 
@@ -327,7 +310,7 @@ using namespace medusa;
 extern "C" size_t medusa_linear_workspace_size(int T, int K, int Nout) {
   if (T < 1 || K < 1 || Nout < 1) return 0;
   const LinearPlan L = linear_plan(T, K, Nout);
-  return L.S > 1 ? align_up(L.part_bytes, 256) + L.counter_bytes : 0;
+  return L.part_bytes;
 }
 
 extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
@@ -358,12 +341,15 @@ extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, in
   p.stage_bytes = L.stage_bytes;
   p.y = static_cast<uint16_t*>(y);
   p.part = L.S > 1 ? static_cast<float*>(ws) : nullptr;
-  p.counters = L.S > 1 ? reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(L.part_bytes, 256)) : nullptr;
   p.d_status = d_status;
-  if (L.S > 1 && cudaMemsetAsync(p.counters, 0, L.counter_bytes, s) != cudaSuccess) return MEDUSA_ERR_CUDA;
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lin::kSmemBytes) !=
       cudaSuccess)
     return MEDUSA_ERR_CUDA;
   launch_pdl(linear_tc_kernel, dim3(L.grid), dim3(lin::kThreads), lin::kSmemBytes, s, mw, mx, p);
+  if (L.S > 1) {
+    const size_t outs = (size_t)T * Nout;
+    launch_pdl(linear_reduce_kernel, dim3((unsigned)((outs + 255) / 256)), dim3(256), 0, s,
+               static_cast<const float*>(ws), p.y, T, Nout, L.TN, L.mtiles, L.S);
+  }
   return launch_status();
 }
