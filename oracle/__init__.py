@@ -9,4 +9,4 @@ Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 tiny inputs, and the worked fixtures under ``tests/golden/``).
 """
 from . import oracle, topology  # noqa: F401
-from .oracle import build, heads, kv_compact, linear, topk_f32, tree_attention, tree_rope, typical_accept  # noqa: F401
+from .oracle import build, head_loss, heads, kv_compact, linear, topk_f32, tree_attention, tree_rope, typical_accept  # noqa: F401

@@ -378,3 +378,75 @@ int orc_tree_rope(const void* x, int dt, const int32_t* pos, int nl, int B, int 
       }
   return 0;
 }
+
+/*
+ * Medusa-1 head loss and its gradient with respect to the head logits.
+ * Review page, section "方法细节" (training recipe): with the backbone frozen,
+ * only the heads train, on L1 = -sum_{k=1..K} lambda_k log p_t^(k)(y_{t+k+1}),
+ * lambda_k = 0.8^k (here decay^k): head k, read at position t, is scored on
+ * the token k + 1 places ahead.
+ *
+ * Readings: the loss of head k is the mean over the counted positions of the
+ * batch (the mean cross entropy of the guide's training loop, "Medusa 多解码头
+ * 推理加速全解析", training section), and L1 is the lambda-weighted sum of
+ * these means.  Position t of sequence b counts for head k when t + k + 1 < S
+ * and its target y[b][t+k+1] is not negative (a negative target marks padding
+ * and is skipped); a head with no counted position has loss 0.
+ *
+ * logits [K][B][S][V] (fp32 or bf16 bits), head k stored at index k - 1;
+ * tokens [B][S].  Outputs: counts[K] (n_k), loss[K + 1] (the K means, then
+ * L1), row_loss[K][B][S] (-log p of the target, 0 where not counted) and, when
+ * dlogits is not NULL, dL1/dz = lambda_k / n_k * (softmax(z) - onehot(y)) on
+ * counted rows, 0 elsewhere.  counts_in, when not NULL, replaces the counts as
+ * the normaliser (a slice of sequences cut from a larger batch).
+ * Returns 2 when a target is >= V.
+ */
+int orc_head_loss(const void* logits, int dt, const int32_t* tokens, int K, int B, int S, int V, double decay,
+                  const int32_t* counts_in, int32_t* counts, double* loss, double* row_loss, double* dlogits) {
+  if (K < 1 || B < 1 || S < 1 || V < 1) return 1;
+  for (size_t i = 0; i < (size_t)B * S; ++i)
+    if (tokens[i] >= V) return 2;
+  for (int k = 1; k <= K; ++k) {
+    int n = 0;
+    for (int b = 0; b < B; ++b)
+      for (int t = 0; t + k + 1 < S; ++t)
+        if (tokens[(size_t)b * S + t + k + 1] >= 0) ++n;
+    counts[k - 1] = counts_in ? counts_in[k - 1] : n;
+  }
+  double* row = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!row) return 1;
+  double total = 0.0;
+  for (int k = 1; k <= K; ++k) {
+    const double lambda = pow(decay, (double)k);
+    const int n = counts[k - 1];
+    double sum = 0.0;
+    for (int b = 0; b < B; ++b)
+      for (int t = 0; t < S; ++t) {
+        const size_t r = ((size_t)(k - 1) * B + b) * S + t;
+        const int y = t + k + 1 < S ? tokens[(size_t)b * S + t + k + 1] : -1;
+        double* g = dlogits ? dlogits + r * V : NULL;
+        if (y < 0 || n <= 0) {
+          row_loss[r] = 0.0;
+          if (g) memset(g, 0, sizeof(double) * (size_t)V);
+          continue;
+        }
+        double m = -INFINITY;
+        for (int v = 0; v < V; ++v) {
+          row[v] = orc_load(logits, dt, r * V + v);
+          if (row[v] > m) m = row[v];
+        }
+        double s = 0.0;
+        for (int v = 0; v < V; ++v) s += exp(row[v] - m);
+        const double lse = m + log(s);
+        row_loss[r] = lse - row[y];
+        sum += row_loss[r];
+        if (g)
+          for (int v = 0; v < V; ++v) g[v] = lambda / n * (exp(row[v] - lse) - (v == y ? 1.0 : 0.0));
+      }
+    loss[k - 1] = n > 0 ? sum / n : 0.0;
+    total += lambda * loss[k - 1];
+  }
+  loss[K] = total;
+  free(row);
+  return 0;
+}

@@ -50,8 +50,9 @@ def lib():
         L.orc_typical_accept.argtypes = [P, P, P, i32, i32, i32, f64, f64, f64, i32, P, P, P, P, P, P]
         L.orc_kv_compact.argtypes = [P, P, P, P, i32, P, P, P, P, P] + [i32] * 7
         L.orc_tree_rope.argtypes = [P, i32, P] + [i32] * 5 + [f64, P]
+        L.orc_head_loss.argtypes = [P, i32, P, i32, i32, i32, i32, f64, P, P, P, P, P]
         for f in (L.orc_heads, L.orc_topk_f32, L.orc_tree_attention, L.orc_typical_accept, L.orc_kv_compact,
-                  L.orc_tree_rope):
+                  L.orc_tree_rope, L.orc_head_loss):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -187,3 +188,25 @@ def linear(x, w):
             return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         return a.astype(np.float64)
     return f64(x) @ f64(w).T
+
+
+def head_loss(logits, tokens, decay: float = 0.8, grad: bool = True, counts=None):
+    """Medusa-1 head loss over logits [K, B, S, V] (float32 or bf16 bits) and
+    tokens [B, S]: head k (stored at k - 1) at position t is scored on token
+    t + k + 1; lambda_k = decay^k.  Returns dict(loss [K] means, total (L1),
+    counts [K], row_loss [K, B, S], dlogits [K, B, S, V] or None), float64.
+    ``counts`` replaces the per-head normalisers (a slice of a larger batch)."""
+    logits = np.ascontiguousarray(logits)
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    K, B, S, V = logits.shape
+    assert tokens.shape == (B, S)
+    cin = None if counts is None else np.ascontiguousarray(counts, np.int32)
+    cnt = np.empty(K, np.int32)
+    loss = np.empty(K + 1, np.float64)
+    rows = np.empty((K, B, S), np.float64)
+    g = np.empty(logits.shape, np.float64) if grad else None
+    rc = lib().orc_head_loss(_p(logits), _dt(logits), _p(tokens), K, B, S, V, float(decay), _p(cin), _p(cnt),
+                             _p(loss), _p(rows), _p(g))
+    if rc:
+        raise ValueError(f"orc_head_loss rejected its arguments ({rc})")
+    return dict(loss=loss[:K], total=float(loss[K]), counts=cnt, row_loss=rows, dlogits=g)

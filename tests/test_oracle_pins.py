@@ -653,3 +653,128 @@ def test_linear_identity_weight_and_rank_one_closed_form():
     y = oracle.linear(x1, w1)
     want = np.outer(x1.astype(np.float64) @ b.astype(np.float64), a.astype(np.float64))
     np.testing.assert_allclose(y, want, rtol=1e-6)
+
+
+# ----------------------------------------------------------------------------- Medusa-1 head loss
+
+def _torch_head_loss(z, y, decay):
+    """The head loss as the library composes it: for head k (1-based) the logits at
+    positions 0 .. S-k-2 against the tokens k + 1 places ahead, torch's mean cross
+    entropy with negative targets ignored, weighted by decay^k and summed."""
+    zt = torch.tensor(z.astype(np.float64), requires_grad=True)
+    K, B, S, V = z.shape
+    yt = torch.tensor(y.astype(np.int64))
+    total = zt.new_zeros(())
+    per_head = []
+    for k in range(1, K + 1):
+        if S - k - 1 <= 0:
+            per_head.append(0.0)
+            continue
+        logits = zt[k - 1, :, :S - k - 1].reshape(-1, V)
+        target = yt[:, k + 1:].reshape(-1).clone()
+        target[target < 0] = -100
+        if (target >= 0).sum() == 0:
+            per_head.append(0.0)
+            continue
+        ce = torch.nn.functional.cross_entropy(logits, target, ignore_index=-100, reduction="mean")
+        per_head.append(float(ce.detach()))
+        total = total + decay ** k * ce
+    total.backward()
+    return np.array(per_head), float(total), zt.grad.numpy()
+
+
+@pytest.mark.parametrize("K,B,S,V,decay", [(3, 2, 9, 7, 0.8), (4, 1, 6, 11, 0.8), (2, 3, 5, 4, 0.5)])
+def test_head_loss_matches_torch_cross_entropy_and_autograd(K, B, S, V, decay):
+    """Paper review, "方法细节": L1 = -sum_k lambda_k log p^(k)_t(y_{t+k+1}),
+    lambda_k = 0.8^k.  Per-head means and the gradient against torch's cross
+    entropy and autograd in float64 (ignored targets included)."""
+    rng = np.random.default_rng(K * 100 + S)
+    z = _f32(rng.standard_normal((K, B, S, V)) * 2)
+    y = rng.integers(0, V, (B, S)).astype(np.int32)
+    y[0, -1] = -1  # one padded target
+    r = oracle.head_loss(z, y, decay)
+    ce, total, grad = _torch_head_loss(z, y, decay)
+    np.testing.assert_allclose(r["loss"], ce, rtol=1e-12, atol=1e-14)
+    assert abs(r["total"] - total) <= 1e-12 * abs(total)
+    np.testing.assert_allclose(r["dlogits"], grad, rtol=1e-10, atol=1e-15)
+
+
+def test_head_loss_uniform_logits_closed_form():
+    """Equal logits: every head's loss is ln V, L1 = ln V * sum_k decay^k, and each
+    counted row's gradient is lambda_k / n_k (1/V - onehot(target))."""
+    K, B, S, V = 3, 2, 7, 10
+    z = np.full((K, B, S, V), 0.375, np.float32)
+    y = (np.arange(B * S).reshape(B, S) % V).astype(np.int32)
+    r = oracle.head_loss(z, y)
+    np.testing.assert_allclose(r["loss"], math.log(V), rtol=1e-14)
+    assert abs(r["total"] - math.log(V) * sum(0.8 ** k for k in range(1, K + 1))) < 1e-13
+    for k in range(1, K + 1):
+        n = B * (S - k - 1)
+        assert r["counts"][k - 1] == n
+        for b in range(B):
+            for t in range(S):
+                g = r["dlogits"][k - 1, b, t]
+                if t + k + 1 >= S:
+                    assert not g.any()
+                    continue
+                want = np.full(V, 0.8 ** k / n / V)
+                want[y[b, t + k + 1]] -= 0.8 ** k / n
+                np.testing.assert_allclose(g, want, rtol=1e-13, atol=1e-17)
+
+
+def test_head_loss_gradient_matches_finite_differences():
+    """Central differences of L1 in float64 on logits that are multiples of 2^-8,
+    perturbed by 2^-12 (both exact in fp32)."""
+    rng = np.random.default_rng(5)
+    K, B, S, V = 2, 2, 6, 5
+    z = _f32(np.round(rng.standard_normal((K, B, S, V)) * 256) / 256)
+    y = rng.integers(0, V, (B, S)).astype(np.int32)
+    g = oracle.head_loss(z, y)["dlogits"]
+    h = 2.0 ** -12
+    for _ in range(25):
+        i = tuple(int(rng.integers(0, n)) for n in z.shape)
+        zp, zm = z.copy(), z.copy()
+        zp[i] += h
+        zm[i] -= h
+        fd = (oracle.head_loss(zp, y, grad=False)["total"] - oracle.head_loss(zm, y, grad=False)["total"]) / (2 * h)
+        assert abs(fd - g[i]) <= 1e-6 * max(1e-3, abs(g[i]))
+
+
+def test_head_loss_ignored_targets_short_sequences_and_bf16():
+    rng = np.random.default_rng(9)
+    K, B, S, V = 3, 2, 4, 6
+    z = _f32(rng.standard_normal((K, B, S, V)))
+    y = rng.integers(0, V, (B, S)).astype(np.int32)
+    # S = 4: head 3 has no position (t + 4 < 4 never holds); head 2 only t = 0
+    r = oracle.head_loss(z, y)
+    assert list(r["counts"]) == [2 * 2, 2 * 1, 0] and r["loss"][2] == 0.0
+    assert not r["dlogits"][2].any()
+    # every target padded: nothing counted, zero loss and gradient
+    r = oracle.head_loss(z, np.full((B, S), -1, np.int32))
+    assert r["total"] == 0.0 and not r["dlogits"].any() and not r["counts"].any()
+    # a target past the vocabulary is rejected
+    bad = y.copy()
+    bad[1, 3] = V
+    with pytest.raises(ValueError):
+        oracle.head_loss(z, bad)
+    # bf16 logits are read as their exact values
+    zb = wl.to_bf16_bits(z)
+    rb = oracle.head_loss(zb, y)
+    rf = oracle.head_loss(wl.bf16_bits_to_f32(zb), y)
+    np.testing.assert_array_equal(rb["dlogits"], rf["dlogits"])
+    # gradient rows sum to zero (softmax minus a one-hot)
+    np.testing.assert_allclose(rb["dlogits"].sum(-1), 0.0, atol=1e-16)
+
+
+def test_head_loss_counts_override_splits_a_batch():
+    """Running two halves of a batch with the whole batch's counts gives the whole
+    batch's gradient rows and per-head means that add up."""
+    rng = np.random.default_rng(11)
+    K, B, S, V = 2, 4, 7, 9
+    z = _f32(rng.standard_normal((K, B, S, V)))
+    y = rng.integers(0, V, (B, S)).astype(np.int32)
+    full = oracle.head_loss(z, y)
+    lo = oracle.head_loss(z[:, :2], y[:2], counts=full["counts"])
+    hi = oracle.head_loss(z[:, 2:], y[2:], counts=full["counts"])
+    np.testing.assert_array_equal(np.concatenate([lo["dlogits"], hi["dlogits"]], 1), full["dlogits"])
+    np.testing.assert_allclose(lo["loss"] + hi["loss"], full["loss"], rtol=1e-14)
