@@ -172,7 +172,11 @@ def run_ours(args, c):
                 "attention": lambda: vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"],
                                                   stream),
                 "accept": lambda: vs.accept(d["logits"], stream),
-                "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}[args.profile]
+                "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}.get(args.profile)
+        if args.profile == "head_loss":  # one sequence of 512 tokens: 262 MB of logits (above L2)
+            lc, z, y = loss_inputs(dev, "f32", B=1, S=512)
+            gz = torch.empty_like(z)
+            call = lambda: mg.medusa_head_loss(z, y, lc["decay"], dlogits=gz, stream=stream)  # noqa: E731
         for _ in range(args.steps):
             call()
         torch.cuda.synchronize()
@@ -248,6 +252,7 @@ def run_ours(args, c):
     del rq, rk, flush
     calib = time_calibration(mg, vs, c, N, K, stream, dev)
     linear = time_linear(mg, c, stream, dev, min(K, 50))
+    head_loss = time_head_loss(mg, stream, dev, min(K, 20))
 
     ms_per_step = elapsed_ms / K
     value = job_steps_per_s(ms_per_step, world)
@@ -274,7 +279,8 @@ def run_ours(args, c):
                 "config": config_json(c, N),
                 "accepted_tok_per_s": round(value * c["B"] * accept_len, 2), "mean_accept_len": accept_len,
                 "per_call_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
-                "roofline": roof, "rooflines": rooflines, "calibration": calib, "linear": linear, "e2e": e2e,
+                "roofline": roof, "rooflines": rooflines, "calibration": calib, "linear": linear,
+                "head_loss": head_loss, "e2e": e2e,
                 "cpu_baseline": cpu,
                 "gpu_launches": K * vs.launches_per_step(), "clocks": clocks}
         print(json.dumps(line))
@@ -347,6 +353,53 @@ def time_linear(mg, c, stream, dev, reps):
                         "tensor_frac": round(flops / us / 1e6 / tflops, 4),
                         "gbs": round(byts / us / 1e3, 1), "hbm_frac": round(byts / us / 1e3 / hbm, 4)}
     del flush
+    return out
+
+
+def loss_inputs(dev, dtype="f32", **over):
+    """The Medusa-1 training batch of the head loss (Vicuna-7B vocabulary, 4 heads,
+    4 sequences of 2048 tokens unless overridden): logits ~ N(0, 2) drawn on the
+    device from a seeded generator, target tokens from the seeded workload."""
+    import torch
+    lc = wl.loss_config("7b", **over)
+    g = torch.Generator(device=dev).manual_seed(lc["cfg_id"])
+    z = torch.randn((lc["K"], lc["B"], lc["S"], lc["V"]), generator=g, device=dev).mul_(2.0)
+    if dtype == "bf16":
+        z = z.to(torch.bfloat16)
+    y = torch.from_numpy(wl.loss_tokens(lc)).to(dev)
+    return lc, z, y
+
+
+def time_head_loss(mg, stream, dev, reps):
+    """Medusa-1 head loss + gradient over the whole training batch (outside the
+    verify step): one read of the logits and one write of their gradient, both
+    larger than L2, so no flush; fp32 and bf16 logits."""
+    import torch
+    hbm, _, _ = _peaks()
+    out = {}
+    for dt in ("f32", "bf16"):
+        lc, z, y = loss_inputs(dev, dt)
+        g = torch.empty_like(z)
+        loss = torch.empty(lc["K"] + 1, dtype=torch.float32, device=dev)
+        ws = torch.empty(mg.lib().medusa_head_loss_workspace_size(lc["K"], lc["B"], lc["S"]), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(3):
+            mg.medusa_head_loss(z, y, lc["decay"], dlogits=g, loss=loss, ws=ws, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i in range(reps):
+            torch.cuda._sleep(200000)  # the host's enqueue of the call is not timed
+            ev[i][0].record(stream)
+            mg.medusa_head_loss(z, y, lc["decay"], dlogits=g, loss=loss, ws=ws, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        us = sum(a.elapsed_time(b) for a, b in ev) / reps * 1e3
+        byts = 2 * z.numel() * z.element_size() + y.numel() * 4
+        out[dt] = {"us": round(us, 1), "algorithmic_bytes": byts, "gbs": round(byts / us / 1e3, 1),
+                   "hbm_frac": round(byts / us / 1e3 / hbm, 4),
+                   "loss": [round(float(v), 5) for v in loss.cpu()]}
+        del z, g, y
+    out["batch"] = f"{lc['K']} heads x {lc['B']} x {lc['S']} tokens x V {lc['V']}"
+    out["peak_gbs"] = hbm
     return out
 
 
@@ -525,7 +578,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
-    ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope"], default=None,
+    ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope", "head_loss"], default=None,
                     help="run only this call `steps` times after warm-up (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:

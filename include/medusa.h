@@ -355,6 +355,34 @@ medusa_status medusa_topology_greedy_device(const double* acc, int K, int R, int
                                             size_t buf_elems, int32_t* d_meta, medusa_dev_topology* out,
                                             int32_t* d_status, medusa_stream_t stream);
 
+/* ------------------------------------------------------------ (f4) head loss
+ * The Medusa-1 training loss of the K heads and its gradient with respect to
+ * the head logits, in one call (paper review, "方法细节": the backbone is
+ * frozen and only the heads train, on L1 = -sum_{k=1..K} lambda_k
+ * log p_t^(k)(y_{t+k+1}) with lambda_k = 0.8^k; head k read at position t is
+ * scored on the token k + 1 places ahead).
+ *   logits [K][B][S][V] (`dt`: fp32 or bf16), head k at index k - 1;
+ *   tokens [B][S] int32: position t of sequence b counts for head k when
+ *   t + k + 1 < S and tokens[b][t+k+1] >= 0 (a negative target is padding and
+ *   is skipped); a target >= V sets BAD_INDEX and is skipped.
+ *   loss [K + 1] fp32: the mean over the counted positions of -log p of the
+ *   target for each head (0 for a head with none), then L1 = sum_k decay^k
+ *   times that mean.  Sums run in fp32 in a fixed order (deterministic).
+ *   dlogits (`dt`, the layout of logits, or NULL for the loss alone; may be
+ *   logits itself, in place, but must not overlap it otherwise):
+ *   dL1/dz = decay^k / n_k * (softmax(z) - onehot(target)) on counted rows,
+ *   0 on the others (n_k = counted positions of head k).
+ *   row_loss [K][B][S] fp32 or NULL: -log p of the target per position (0
+ *   where not counted).
+ *   1 <= K <= MEDUSA_MAX_HEAD_LOSS_HEADS, K * B * S < 2^31, V >= 1, decay
+ *   finite, logits / dlogits aligned to their element size; the scratch is
+ *   medusa_head_loss_workspace_size(K, B, S) bytes, 16-byte aligned. */
+#define MEDUSA_MAX_HEAD_LOSS_HEADS 32
+size_t medusa_head_loss_workspace_size(int K, int B, int S);
+medusa_status medusa_head_loss(const void* logits, const int32_t* tokens, int K, int B, int S, int V, float decay,
+                               medusa_dtype dt, void* dlogits, float* loss, float* row_loss, void* ws,
+                               size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
+
 /* ------------------------------------------------------------------ status
  * Synchronises `stream`, copies the device status word to *host_code and
  * resets it to 0.  Returns CUDA_ERROR if the stream holds a failed launch. */

@@ -31,6 +31,7 @@ EXPORTS = (
     "medusa_status_check", "medusa_status_string", "medusa_version", "medusa_typical_accept_noalloc",
     "medusa_tree_rope", "medusa_accept_stats", "medusa_acc_update", "medusa_topology_greedy_device_elems",
     "medusa_topology_greedy_device", "medusa_linear_workspace_size", "medusa_linear",
+    "medusa_head_loss_workspace_size", "medusa_head_loss",
 )
 
 
@@ -92,6 +93,8 @@ def lib():
             "medusa_accept_stats": (I, [P, P, P, I, I, I, P, P, P, P]),
             "medusa_linear_workspace_size": (Z, [I, I, I]),
             "medusa_linear": (I, [P, P, P, I, I, I, I, P, Z, P, P]),
+            "medusa_head_loss_workspace_size": (Z, [I, I, I]),
+            "medusa_head_loss": (I, [P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, Z, P, P]),
             "medusa_acc_update": (I, [P, P, P, I, I, ctypes.c_double, P]),
             "medusa_topology_greedy_device_elems": (Z, [I, I]),
             "medusa_topology_greedy_device": (I, [P, I, I, I, P, Z, P, P, P, P]),
@@ -376,6 +379,29 @@ def medusa_linear(x, w, y=None, ws=None, d_status=None, stream=None):
         _ptr(x), _ptr(w), _ptr(y), T, K, Nout, _dtype_code(x), _ptr(ws), 0 if ws is None else ws.numel(),
         _ptr(d_status), _stream(stream)))
     return y
+
+
+def medusa_head_loss(logits, tokens, decay: float = 0.8, grad: bool = True, dlogits=None, loss=None,
+                     row_loss=None, ws=None, d_status=None, stream=None):
+    """Medusa-1 head loss over logits [K, B, S, V] (fp32 / bf16) and tokens [B, S]
+    (int32; negative = padding).  Returns (loss [K + 1] fp32: the K per-head
+    means then L1, dlogits or None).  With grad, dlogits is allocated unless
+    given; pass the logits tensor itself for the in-place gradient."""
+    import torch
+    K, B, S, V = logits.shape
+    if tuple(tokens.shape) != (B, S):
+        raise ValueError("tokens must be [B, S]")
+    if loss is None:
+        loss = torch.empty(K + 1, dtype=torch.float32, device=logits.device)
+    if grad and dlogits is None:
+        dlogits = torch.empty_like(logits)
+    if not grad:
+        dlogits = None
+    ws = _ws(lib().medusa_head_loss_workspace_size(K, B, S), logits.device, ws)
+    _check("medusa_head_loss", lib().medusa_head_loss(
+        _ptr(logits), _ptr(tokens), K, B, S, V, float(decay), _dtype_code(logits), _ptr(dlogits), _ptr(loss),
+        _ptr(row_loss), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(d_status), _stream(stream)))
+    return loss, dlogits
 
 
 def medusa_accept_stats(path_nodes, accept_len, topo: DevTopology, R: int, tested, accepted, d_status=None,

@@ -32,6 +32,14 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
 }
 
+// Two floats to packed bf16 (round to nearest even, hardware conversion); lo in
+// the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // 16-byte streaming load that bypasses L1 (weights are read exactly once).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;

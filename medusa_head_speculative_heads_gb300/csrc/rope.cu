@@ -72,12 +72,6 @@ __device__ __forceinline__ uint4 pack16(const float* f, uint16_t) {
   return make_uint4(u[0], u[1], u[2], u[3]);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Angles of this CTA's token: cs[i] = (cos, sin)(pos * theta_i), the product
 // formed and reduced modulo 2 pi in double.
 __device__ __forceinline__ void rope_angles(float2* cs, double ps, const RopeParams& p) {

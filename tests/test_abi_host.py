@@ -147,4 +147,18 @@ def test_host_validation_rejects_before_launch():
     if L.medusa_linear_workspace_size(64, 4096, 4096):
         assert L.medusa_linear(P(base), P(base * 64), P(base * 128), 64, 4096, 4096, 1, P(base * 256), 16, None,
                                None) == 5
+    # head loss: missing logits, too many heads, unknown dtype, misaligned logits, infinite decay,
+    # a gradient that half-overlaps the logits, workspace missing or short
+    zl, tk, ls, wsp = P(base), P(base * 64), P(base * 96), P(base * 128)
+    HL = L.medusa_head_loss
+    assert HL(None, tk, 4, 2, 8, 64, F(0.8), 0, None, ls, None, wsp, 1 << 20, None, None) == 1
+    assert HL(zl, tk, 33, 2, 8, 64, F(0.8), 0, None, ls, None, wsp, 1 << 20, None, None) == 1
+    assert HL(zl, tk, 4, 2, 8, 64, F(0.8), 7, None, ls, None, wsp, 1 << 20, None, None) == 2
+    assert HL(P(base + 2), tk, 4, 2, 8, 64, F(0.8), 0, None, ls, None, wsp, 1 << 20, None, None) == 1
+    assert HL(zl, tk, 4, 2, 8, 64, F(float("inf")), 0, None, ls, None, wsp, 1 << 20, None, None) == 1
+    assert HL(zl, tk, 4, 2, 8, 64, F(0.8), 0, P(base + 256), ls, None, wsp, 1 << 20, None, None) == 3
+    assert HL(zl, tk, 4, 2, 8, 64, F(0.8), 0, None, ls, None, None, 0, None, None) == 5
+    assert HL(zl, tk, 4, 2, 8, 64, F(0.8), 0, None, ls, None, wsp, 64, None, None) == 5
+    assert L.medusa_head_loss_workspace_size(4, 4, 2048) == 48 + 4 * 4 * 2048 * 4
+    assert L.medusa_head_loss_workspace_size(33, 1, 1) == 0
     assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"

@@ -680,7 +680,7 @@ def _torch_head_loss(z, y, decay):
         per_head.append(float(ce.detach()))
         total = total + decay ** k * ce
     total.backward()
-    return np.array(per_head), float(total), zt.grad.numpy()
+    return np.array(per_head), float(total.detach()), zt.grad.numpy()
 
 
 @pytest.mark.parametrize("K,B,S,V,decay", [(3, 2, 9, 7, 0.8), (4, 1, 6, 11, 0.8), (2, 3, 5, 4, 0.5)])

@@ -188,3 +188,42 @@ def step_inputs(c: dict, N: int, layers=None, rows=None) -> dict:
     return dict(h=hidden(c, rows_l), w1=w1, w2=w2, root_tok=root_tokens(c, rows_l),
                 prefix_len=np.full(len(rows_l), c["L"], np.int32), q=queries(c, N, layers, rows_l),
                 kc=kc, vc=vc, kt=kt, vt=vt, logits=base_logits(c, N, rows_l), rows=rows_l)
+
+
+# ----------------------------------------------------------------- head-loss (training) workload
+# Medusa-1 trains the heads on the frozen backbone's hidden states over whole
+# sequences.  The synthetic stand-in for a training batch: K heads' logits over
+# B sequences of S tokens (the Vicuna-7B vocabulary) ~ N(0, 2) in fp32 and
+# target tokens uniform over the vocabulary.  No training data is reproduced.
+T_LOSS_TOK, T_LOSS_LOGITS = 13, 14
+
+LOSS_CONFIGS = {
+    "tiny": dict(cfg_id=11, K=2, B=2, S=16, V=1024, decay=0.8),
+    "7b": dict(cfg_id=12, K=4, B=4, S=2048, V=32000, decay=0.8),
+}
+
+
+def loss_config(name: str, **over) -> dict:
+    c = dict(LOSS_CONFIGS[name])
+    c["name"] = name
+    c.update(over)
+    return c
+
+
+def loss_tokens(c: dict) -> np.ndarray:
+    """Target tokens [B, S] int32, one seed per sequence."""
+    return np.stack([rng(c["cfg_id"], T_LOSS_TOK, 0, b).integers(0, c["V"], c["S"], dtype=np.int32)
+                     for b in range(c["B"])])
+
+
+def loss_logits(c: dict, k: int, b: int, dtype: str = "f32") -> np.ndarray:
+    """Logits [S, V] of head k (1-based) for sequence b ~ N(0, 2)."""
+    return _normal(rng(c["cfg_id"], T_LOSS_LOGITS, k, b), (c["S"], c["V"]), 2.0, dtype)
+
+
+def loss_logits_all(c: dict, dtype: str = "f32") -> np.ndarray:
+    """Logits [K, B, S, V] of every head and sequence."""
+    jobs = [(k, b) for k in range(1, c["K"] + 1) for b in range(c["B"])]
+    with _cf.ThreadPoolExecutor(_threads()) as ex:
+        parts = list(ex.map(lambda kb: loss_logits(c, kb[0], kb[1], dtype), jobs))
+    return np.stack(parts).reshape(c["K"], c["B"], c["S"], c["V"])
