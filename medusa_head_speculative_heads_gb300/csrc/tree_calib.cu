@@ -70,44 +70,106 @@ __global__ void acc_update_kernel(double* __restrict__ acc, const unsigned long 
 
 // ------------------------------------------------------------------ greedy tree
 
+typedef unsigned __int128 u128;
+
+// Canonical key of a tree path: (length << 80) | ranks, 5 bits per level with
+// the first level most significant (R <= 32, depth <= 16).  Keys order like
+// the canonical order: shorter paths first, then lexicographic.
+__device__ __forceinline__ u128 child_key(u128 parent_key, int parent_len, int r) {
+  return parent_key + ((u128)1 << 80) + ((u128)(unsigned)r << (5 * (MEDUSA_MAX_DEPTH - 1 - parent_len)));
+}
+__device__ __forceinline__ int key_rank(u128 key, int level) {
+  return (int)((key >> (5 * (MEDUSA_MAX_DEPTH - 1 - level))) & 31u);
+}
+
 struct GreedyState {
-  int8_t path[MEDUSA_MAX_NODES][MEDUSA_MAX_DEPTH];
-  int len[MEDUSA_MAX_NODES];
+  u128 key[MEDUSA_MAX_NODES];       // canonical key of chosen node i
   double score[MEDUSA_MAX_NODES];
+  double best_sc[MEDUSA_MAX_NODES]; // best not-yet-chosen child of chosen node i: score
+  int len[MEDUSA_MAX_NODES];
   uint32_t kids[MEDUSA_MAX_NODES];  // bit r: child with rank r already chosen
   int pchosen[MEDUSA_MAX_NODES];    // chosen index of the parent
   int canon[MEDUSA_MAX_NODES];      // canonical index of chosen node i
+  int best_r[MEDUSA_MAX_NODES];     // and its rank (-1: none left)
   double acc[MEDUSA_MAX_DEPTH * MEDUSA_MAX_TOPK];
 };
 
-// Canonical order of chosen node a's child with rank ra vs chosen node b's
-// child with rank rb: shorter path first, then lexicographic.
-__device__ __forceinline__ bool child_less(const GreedyState& s, int a, int ra, int b, int rb) {
-  const int la = s.len[a] + 1, lb = s.len[b] + 1;
-  if (la != lb) return la < lb;
-  for (int j = 0; j < la; ++j) {
-    const int x = j < la - 1 ? s.path[a][j] : ra;
-    const int y = j < lb - 1 ? s.path[b][j] : rb;
-    if (x != y) return x < y;
+// A frontier candidate: child of chosen node a with rank r (a < 0: none).
+struct Cand {
+  double sc;
+  u128 key;
+  int a, r;
+};
+
+// Greedy preference of candidate x over y: scores within a relative 1e-12 are
+// ties, broken by canonical order (the key).
+//
+// Scores are products of table entries in [0, 1], so non-negative: their bit
+// patterns order like their values, and the integer distance d of the patterns
+// counts units in the last place.  Two normal doubles d ulps apart differ by at
+// most d 2^-52 and (within a factor of two of each other) at least d 2^-54 of
+// the larger, so d <= 4000 is always inside the 1e-12 window and d >= 20000
+// always outside; only the band between, zeros and subnormals take the double
+// test (double arithmetic is slow on this GPU; the outcome is the same).
+__device__ __forceinline__ bool beats(const Cand& x, const Cand& y) {
+  if (y.a < 0) return x.a >= 0;
+  if (x.a < 0) return false;
+  const long long ia = __double_as_longlong(x.sc), ib = __double_as_longlong(y.sc);
+  const long long d = ia > ib ? ia - ib : ib - ia;
+  bool tie;
+  if ((ia >> 52) == 0 || (ib >> 52) == 0 || (d > 4000 && d < 20000))
+    tie = fabs(x.sc - y.sc) <= 1e-12 * fmax(fabs(x.sc), fabs(y.sc));
+  else
+    tie = d <= 4000;
+  if (tie) return x.key < y.key;
+  return ia > ib;
+}
+
+__device__ __forceinline__ u128 shfl_xor_u128(u128 v, int o) {
+  const unsigned long long lo = (unsigned long long)v, hi = (unsigned long long)(v >> 64);
+  return ((u128)__shfl_xor_sync(0xffffffffu, hi, o) << 64) | __shfl_xor_sync(0xffffffffu, lo, o);
+}
+__device__ __forceinline__ u128 shfl_u128(u128 v, int src) {
+  const unsigned long long lo = (unsigned long long)v, hi = (unsigned long long)(v >> 64);
+  return ((u128)__shfl_sync(0xffffffffu, hi, src) << 64) | __shfl_sync(0xffffffffu, lo, src);
+}
+
+// Warp argmax under `beats`; lane 0's winner is the result, broadcast.
+__device__ __forceinline__ void warp_best(Cand& c) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    Cand y;
+    y.sc = __shfl_xor_sync(0xffffffffu, c.sc, o);
+    y.key = shfl_xor_u128(c.key, o);
+    y.a = __shfl_xor_sync(0xffffffffu, c.a, o);
+    y.r = __shfl_xor_sync(0xffffffffu, c.r, o);
+    if (beats(y, c)) c = y;
   }
-  return false;
+  c.sc = __shfl_sync(0xffffffffu, c.sc, 0);
+  c.key = shfl_u128(c.key, 0);
+  c.a = __shfl_sync(0xffffffffu, c.a, 0);
+  c.r = __shfl_sync(0xffffffffu, c.r, 0);
 }
 
-// Canonical order of two chosen nodes.
-__device__ __forceinline__ bool node_less(const GreedyState& s, int a, int b) {
-  if (s.len[a] != s.len[b]) return s.len[a] < s.len[b];
-  for (int j = 0; j < s.len[a]; ++j)
-    if (s.path[a][j] != s.path[b][j]) return s.path[a][j] < s.path[b][j];
-  return false;
-}
-
-// Greedy preference of candidate (sa; child of a with rank ra) over (sb; b, rb):
-// scores within a relative 1e-12 are ties, broken by canonical order.
-__device__ __forceinline__ bool beats(const GreedyState& s, double sa, int a, int ra, double sb, int b, int rb) {
-  if (b < 0) return a >= 0;
-  if (a < 0) return false;
-  if (fabs(sa - sb) <= 1e-12 * fmax(fabs(sa), fabs(sb))) return child_less(s, a, ra, b, rb);
-  return sa > sb;
+// One warp: the best child of chosen node a that is not chosen yet (lane = rank).
+__device__ __forceinline__ void refresh_best_child(GreedyState& s, int a, int K, int R, int lane) {
+  Cand c;
+  c.sc = 0.0;
+  c.key = 0;
+  c.a = -1;
+  c.r = -1;
+  const int la = s.len[a];
+  if (lane < R && la < K && !((s.kids[a] >> lane) & 1u)) {
+    c.sc = s.score[a] * s.acc[la * R + lane];
+    c.key = child_key(s.key[a], la, lane);
+    c.a = a;
+    c.r = lane;
+  }
+  warp_best(c);
+  if (lane == 0) {
+    s.best_sc[a] = c.sc;
+    s.best_r[a] = c.r;
+  }
 }
 
 // One CTA.  Device buffer: parent[n], depth[n], rank[n], retrieve[n][K + 1].
@@ -117,8 +179,6 @@ greedy_tree_kernel(const double* __restrict__ acc_in, int K, int R, int n_nodes,
                    int32_t* __restrict__ meta, int32_t* d_status) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GreedyState& s = *reinterpret_cast<GreedyState*>(smem_raw);
-  __shared__ double w_sc[kGreedyThreads / 32];
-  __shared__ int w_a[kGreedyThreads / 32], w_r[kGreedyThreads / 32];
   __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
@@ -134,6 +194,7 @@ greedy_tree_kernel(const double* __restrict__ acc_in, int K, int R, int n_nodes,
     s.acc[i] = v;
   }
   if (tid == 0) {
+    s.key[0] = 0;
     s.len[0] = 0;
     s.score[0] = 1.0;
     s.kids[0] = 0u;
@@ -142,61 +203,51 @@ greedy_tree_kernel(const double* __restrict__ acc_in, int K, int R, int n_nodes,
   __syncthreads();
   if (tid == 0 && s_bad) set_status(d_status, MEDUSA_DEV_BAD_INDEX);
 
-  for (int c = 1; c < n_nodes; ++c) {
-    // Best frontier candidate: (chosen node a, rank r) not yet chosen.
-    double best_s = 0.0;
-    int best_a = -1, best_r = -1;
-    for (int idx = tid; idx < c * R; idx += kGreedyThreads) {
-      const int a = idx / R, r = idx - a * R;
-      if (s.len[a] >= K || ((s.kids[a] >> r) & 1u)) continue;
-      const double sc = s.score[a] * s.acc[s.len[a] * R + r];
-      if (beats(s, sc, a, r, best_s, best_a, best_r)) {
-        best_s = sc;
-        best_a = a;
-        best_r = r;
+  // Greedy growth, one warp.  Every chosen node keeps its best child not chosen
+  // yet; a round takes the best of those (the frontier's best under `beats`),
+  // adds it, and refreshes the best child of the new node and of its parent.
+  if (warp == 0) {
+    refresh_best_child(s, 0, K, R, lane);
+    __syncwarp();
+    for (int c = 1; c < n_nodes; ++c) {
+      Cand best;
+      best.sc = 0.0;
+      best.key = 0;
+      best.a = -1;
+      best.r = -1;
+      for (int a = lane; a < c; a += 32) {
+        Cand x;
+        x.r = s.best_r[a];
+        if (x.r < 0) continue;
+        x.sc = s.best_sc[a];
+        x.key = child_key(s.key[a], s.len[a], x.r);
+        x.a = a;
+        if (beats(x, best)) best = x;
       }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const double s2 = __shfl_xor_sync(0xffffffffu, best_s, o);
-      const int a2 = __shfl_xor_sync(0xffffffffu, best_a, o);
-      const int r2 = __shfl_xor_sync(0xffffffffu, best_r, o);
-      if (beats(s, s2, a2, r2, best_s, best_a, best_r)) {
-        best_s = s2;
-        best_a = a2;
-        best_r = r2;
-      }
-    }
-    if (lane == 0) {
-      w_sc[warp] = best_s;
-      w_a[warp] = best_a;
-      w_r[warp] = best_r;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      for (int w = 1; w < kGreedyThreads / 32; ++w)
-        if (beats(s, w_sc[w], w_a[w], w_r[w], best_s, best_a, best_r)) {
-          best_s = w_sc[w];
-          best_a = w_a[w];
-          best_r = w_r[w];
-        }
+      warp_best(best);
       // The host checks that n_nodes nodes exist, so a candidate is always found.
-      const int a = best_a < 0 ? 0 : best_a, r = best_r < 0 ? 0 : best_r;
-      for (int j = 0; j < s.len[a]; ++j) s.path[c][j] = s.path[a][j];
-      s.path[c][s.len[a]] = (int8_t)r;
-      s.len[c] = s.len[a] + 1;
-      s.score[c] = best_s;
-      s.kids[c] = 0u;
-      s.kids[a] |= 1u << r;
-      s.pchosen[c] = a;
+      const int a = best.a < 0 ? 0 : best.a, r = best.r < 0 ? 0 : best.r;
+      if (lane == 0) {
+        s.key[c] = best.key;
+        s.len[c] = s.len[a] + 1;
+        s.score[c] = best.sc;
+        s.kids[c] = 0u;
+        s.kids[a] |= 1u << r;
+        s.pchosen[c] = a;
+      }
+      __syncwarp();
+      refresh_best_child(s, c, K, R, lane);
+      refresh_best_child(s, a, K, R, lane);
+      __syncwarp();
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // Canonical order, then the device topology arrays.
   for (int t = tid; t < n_nodes; t += kGreedyThreads) {
     int k = 0;
-    for (int u = 0; u < n_nodes; ++u) k += node_less(s, u, t) ? 1 : 0;
+    const u128 kt = s.key[t];
+    for (int u = 0; u < n_nodes; ++u) k += s.key[u] < kt ? 1 : 0;
     s.canon[t] = k;
   }
   __syncthreads();
@@ -209,7 +260,7 @@ greedy_tree_kernel(const double* __restrict__ acc_in, int K, int R, int n_nodes,
     const int ci = s.canon[t];
     parent[ci] = t == 0 ? -1 : s.canon[s.pchosen[t]];
     depth[ci] = s.len[t];
-    rankv[ci] = s.len[t] ? s.path[t][s.len[t] - 1] : -1;
+    rankv[ci] = s.len[t] ? key_rank(s.key[t], s.len[t] - 1) : -1;
   }
   // Leaves (no chosen child) in canonical order: row = canonical leaves before it.
   for (int t = tid; t < n_nodes; t += kGreedyThreads) {
@@ -227,7 +278,7 @@ greedy_tree_kernel(const double* __restrict__ acc_in, int K, int R, int n_nodes,
     for (int t = 0; t < n_nodes; ++t) {
       md = max(md, s.len[t]);
       leaves += s.kids[t] ? 0 : 1;
-      if (s.len[t]) mr = max(mr, s.path[t][s.len[t] - 1] + 1);
+      if (s.len[t]) mr = max(mr, key_rank(s.key[t], s.len[t] - 1) + 1);
     }
     meta[0] = n_nodes;
     meta[1] = md;
