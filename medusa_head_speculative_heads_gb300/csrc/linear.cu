@@ -12,10 +12,10 @@
 // Tiles of 128 output features (the weight rows, MMA M = 128) by up to 256
 // tokens (MMA N = TN).  Few tiles (small T, narrow layers) would leave SMs idle
 // while the weights stream from HBM, so each tile's K range is split S ways
-// into fp32 partials, which a second kernel adds in a fixed order (one thread
-// per output element, every SM busy; deterministic).  Roles (256 threads, persistent over the units):
-// warp 0 lane 0 issues TMA loads of the W and x boxes (128-byte swizzle) into a
-// 4- to 8-stage ring; warp 1 owns TMEM and lane 0 issues the MMAs into one of
+// into fp32 partials, which a second kernel adds in a fixed order (four
+// output features per thread; deterministic).  Roles (256 threads, persistent
+// over the units): warp 0 lane 0 issues TMA loads of the W and x boxes
+// (128-byte swizzle) into a 4- to 12-stage ring (216 KB); warp 1 owns TMEM and lane 0 issues the MMAs into one of
 // two 256-column accumulators; warps 4-7 read the accumulator 32 columns at a
 // time (one feature row per thread) and write y or the partial.  Every wait is
 // bounded; a timeout sets MEDUSA_DEV_TIMEOUT, drains and frees TMEM.
@@ -33,10 +33,12 @@ using namespace sm100;
 namespace lin {
 
 constexpr int kThreads = 256;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 14;
+constexpr int kMaxSplit = 16;
 constexpr uint32_t kATile = 16384;        // 128 W rows x 128 bytes
-constexpr uint32_t kRingBytes = 196608;   // 192 KB of stages
-constexpr uint32_t kSmemBytes = kRingBytes + 256 + 1024;
+constexpr uint32_t kRingBytes = 221184;   // 216 KB of stages
+constexpr uint32_t kBarBytes = 512;
+constexpr uint32_t kSmemBytes = kRingBytes + kBarBytes + 1024;  // + alignment slack of the base
 constexpr uint32_t kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
@@ -52,6 +54,7 @@ struct Params {
 struct Bars {
   uint64_t full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2], drain;
 };
+static_assert(sizeof(Bars) <= kBarBytes, "barriers overflow their slot");
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const bool ok = mbar_wait_bounded(bar, parity, abort, kWaitNs);
@@ -214,20 +217,42 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 }
 
 // Split K: y[t][n] = bf16(sum over s of the partials), s in order.  One thread
-// per output element, feature fastest (coalesced partial reads and y writes).
+// per 4 consecutive output features of a token: the partials are feature
+// fastest, so each split is one 16-byte load (all S issued before the first
+// add) and the result one 8-byte store (element stores at a ragged feature
+// tail or when Nout is not a multiple of 4).
 __global__ void __launch_bounds__(256)
 linear_reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, int T, int Nout, int TN,
                      int mtiles, int S) {
   pdl_wait();
   pdl_trigger();
+  const int nq = (Nout + 3) >> 2;  // feature quads per token
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (size_t)T * Nout) return;
-  const int t = (int)(i / Nout), n = (int)(i - (size_t)t * Nout);
+  if (i >= (size_t)T * nq) return;
+  const int t = (int)(i / nq), n = (int)(i - (size_t)t * nq) * 4;
   const int tile = (t / TN) * mtiles + n / 128, col = t % TN, row = n % 128;
-  const float* src = part + (((size_t)tile * S) * TN + col) * 128 + row;
-  float acc = 0.f;
-  for (int s = 0; s < S; ++s) acc += __ldcg(src + (size_t)s * TN * 128);
-  y[i] = (uint16_t)f32_to_bf16_bits(acc);
+  const float4* src = reinterpret_cast<const float4*>(part + (((size_t)tile * S) * TN + col) * 128 + row);
+  const size_t step = (size_t)TN * 128 / 4;  // one split, in float4
+  float4 v[lin::kMaxSplit];
+#pragma unroll
+  for (int s = 0; s < lin::kMaxSplit; ++s)
+    if (s < S) v[s] = __ldcg(src + s * step);
+  float a0 = v[0].x, a1 = v[0].y, a2 = v[0].z, a3 = v[0].w;
+#pragma unroll
+  for (int s = 1; s < lin::kMaxSplit; ++s)
+    if (s < S) {
+      a0 += v[s].x;
+      a1 += v[s].y;
+      a2 += v[s].z;
+      a3 += v[s].w;
+    }
+  uint16_t* out = y + (size_t)t * Nout + n;
+  if ((Nout & 3) == 0) {
+    *reinterpret_cast<uint2*>(out) = make_uint2(bf16x2_rn(a0, a1), bf16x2_rn(a2, a3));
+  } else {
+    const float a[4] = {a0, a1, a2, a3};
+    for (int j = 0; j < 4 && n + j < Nout; ++j) out[j] = (uint16_t)f32_to_bf16_bits(a[j]);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -282,7 +307,7 @@ static LinearPlan linear_plan(int T, int K, int Nout) {
   const double t_tile = fmax(2.0 * 128 * L.TN * (double)K / sm_flops, 128.0 * 2 * (double)K / sm_bw);
   L.S = 1;
   int max_s = L.kblocks / 4 > 1 ? L.kblocks / 4 : 1;  // at least 4 K blocks per unit
-  if (max_s > 16) max_s = 16;
+  if (max_s > lin::kMaxSplit) max_s = lin::kMaxSplit;
   double best = 1e30;
   for (int S = 1; S <= max_s; ++S) {
     const double rounds = (double)((tiles * S + sms - 1) / sms);
@@ -347,8 +372,8 @@ extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, in
     return MEDUSA_ERR_CUDA;
   launch_pdl(linear_tc_kernel, dim3(L.grid), dim3(lin::kThreads), lin::kSmemBytes, s, mw, mx, p);
   if (L.S > 1) {
-    const size_t outs = (size_t)T * Nout;
-    launch_pdl(linear_reduce_kernel, dim3((unsigned)((outs + 255) / 256)), dim3(256), 0, s,
+    const size_t quads = (size_t)T * ((Nout + 3) / 4);
+    launch_pdl(linear_reduce_kernel, dim3((unsigned)((quads + 255) / 256)), dim3(256), 0, s,
                static_cast<const float*>(ws), p.y, T, Nout, L.TN, L.mtiles, L.S);
   }
   return launch_status();

@@ -44,6 +44,7 @@ SHAPES = [
     (256, 4096, 1000),  # full 256-token tile, ragged feature tail
     (1024, 512, 1024),  # many tiles, several units per CTA
     (40, 520, 136),     # K not a multiple of 64
+    (32, 2048, 1002),   # split K with a feature count that is not a multiple of 4
 ]
 
 
@@ -72,6 +73,24 @@ def test_linear_split_k_is_deterministic_and_reuses_its_workspace(mg):
 def test_linear_vicuna7b_layers_at_64_tree_tokens(mg, K, N):
     T = 64
     x, w = _inputs(T, K, N, K + N)
+    y = mg.medusa_linear(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    _check(to_host(y), oracle.linear(x, w))
+
+
+
+MORE_SHAPES = [
+    (16, 2048, 1152),   # 16-token tile, 9 weight tiles, split K
+    (64, 2048, 640),    # 5 weight tiles, split K
+    (256, 1024, 1408),  # full 256-token tile, 11 weight tiles
+    (1000, 512, 768),   # four token tiles, ragged last one
+    (96, 4096, 2176),   # 96-token tile, split K
+]
+
+
+@pytest.mark.parametrize("T,K,N", MORE_SHAPES, ids=[f"T{t}-K{k}-N{n}" for t, k, n in MORE_SHAPES])
+def test_linear_parity_more_shapes(mg, T, K, N):
+    x, w = _inputs(T, K, N, T + K + N)
     y = mg.medusa_linear(to_dev(x), to_dev(w))
     torch.cuda.synchronize()
     _check(to_host(y), oracle.linear(x, w))
