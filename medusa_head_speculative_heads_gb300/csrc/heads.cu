@@ -61,28 +61,32 @@ __device__ __forceinline__ void fma_chunk(const uint4 (&w)[NR], const float* __r
 }
 
 // One warp: dot products of NR consecutive rows (starting at `row`) with the
-// BB staged vectors.  Lane l reads 16-byte chunks l, l+32, ... of each row,
-// two chunks per row per iteration (2*NR loads in flight per lane).
+// BB staged vectors.  Lane l reads 16-byte chunks l, l+32, ... of each row, U
+// chunks per row per iteration with U * NR ~ 8 loads in flight per lane
+// whatever the row count (a warp left with one or two rows would otherwise
+// walk its rows one latency at a time).  Chunks are accumulated in ascending
+// order in every case.
 template <typename TW, int BB, int NR>
 __device__ __forceinline__ void warp_rows(const TW* __restrict__ W, int C, const float* __restrict__ xs,
                                           int lane, float (&acc)[NR][BB]) {
   constexpr int VEC = Vec16<TW>::n;
   constexpr int STEP = 32 * VEC;
+  constexpr int U = NR >= 4 ? 2 : (8 + NR - 1) / NR;
 #pragma unroll
   for (int i = 0; i < NR; ++i)
 #pragma unroll
     for (int bb = 0; bb < BB; ++bb) acc[i][bb] = 0.f;
   int c = lane * VEC;
-  for (; c + STEP < C; c += 2 * STEP) {
-    uint4 wa[NR], wb[NR];
+  for (; c + (U - 1) * STEP < C; c += U * STEP) {
+    uint4 w[U][NR];
 #pragma unroll
-    for (int i = 0; i < NR; ++i) wa[i] = ldg_stream(W + (size_t)i * C + c);
+    for (int u = 0; u < U; ++u)
 #pragma unroll
-    for (int i = 0; i < NR; ++i) wb[i] = ldg_stream(W + (size_t)i * C + c + STEP);
-    fma_chunk<TW, BB, NR>(wa, xs, C, c, acc);
-    fma_chunk<TW, BB, NR>(wb, xs, C, c + STEP, acc);
+      for (int i = 0; i < NR; ++i) w[u][i] = ldg_stream(W + (size_t)i * C + c + u * STEP);
+#pragma unroll
+    for (int u = 0; u < U; ++u) fma_chunk<TW, BB, NR>(w[u], xs, C, c + u * STEP, acc);
   }
-  if (c < C) {
+  for (; c < C; c += STEP) {
     uint4 wa[NR];
 #pragma unroll
     for (int i = 0; i < NR; ++i) wa[i] = ldg_stream(W + (size_t)i * C + c);
