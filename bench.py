@@ -252,6 +252,7 @@ def run_ours(args, c):
     del rq, rk, flush
     calib = time_calibration(mg, vs, c, N, K, stream, dev)
     linear = time_linear(mg, c, stream, dev, min(K, 50))
+    linear_chain = time_linear_chain(mg, c, stream, dev)
     head_loss = time_head_loss(mg, stream, dev, min(K, 20))
 
     ms_per_step = elapsed_ms / K
@@ -279,7 +280,7 @@ def run_ours(args, c):
                 "config": config_json(c, N),
                 "accepted_tok_per_s": round(value * c["B"] * accept_len, 2), "mean_accept_len": accept_len,
                 "per_call_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
-                "roofline": roof, "rooflines": rooflines, "calibration": calib, "linear": linear,
+                "roofline": roof, "rooflines": rooflines, "calibration": calib, "linear": linear, "linear_verify_pass": linear_chain,
                 "head_loss": head_loss, "e2e": e2e,
                 "cpu_baseline": cpu,
                 "gpu_launches": K * vs.launches_per_step(), "clocks": clocks}
@@ -353,6 +354,50 @@ def time_linear(mg, c, stream, dev, reps):
                         "tensor_frac": round(flops / us / 1e6 / tflops, 4),
                         "gbs": round(byts / us / 1e3, 1), "hbm_frac": round(byts / us / 1e3 / hbm, 4)}
     del flush
+    return out
+
+
+def time_linear_chain(mg, c, stream, dev, reps=10):
+    """The verify pass's linear layers of one Vicuna-7B-shape transformer layer
+    (qkv 4096 -> 12288, o 4096 -> 4096, gate_up 4096 -> 22016, down 11008 -> 4096),
+    two layers' worth of distinct weights (807 MB, above L2) run back to back as
+    a verify pass runs them, over the tree tokens of B = 1, 4 and 16 rows at 64
+    nodes.  Weights are synthetic N(0, 0.02) bf16 drawn on the device."""
+    import torch
+    hbm, tflops, _ = _peaks()
+    H, I = c["H"], 11008
+    shapes = [(H, 3 * H), (H, H), (H, 2 * I), (I, H)]
+    g = torch.Generator(device=dev).manual_seed(1)
+    layers = [(K, N, (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16))
+              for _ in range(2) for K, N in shapes]
+    wbytes = sum(2 * K * N for K, N, _ in layers)
+    out = {"layers": "qkv, o, gate_up, down x 2 (Vicuna-7B shapes)", "weight_bytes": wbytes}
+    for B in (1, 4, 16):
+        T = B * 64
+        xs = {K: torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16) for K in (H, I)}
+        ys = {N: torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _, N in shapes}
+        ws = torch.empty(max(1, max(mg.lib().medusa_linear_workspace_size(T, K, N) for K, N in shapes)),
+                         dtype=torch.uint8, device=dev)
+
+        def chain():
+            for K, N, w in layers:
+                mg.medusa_linear(xs[K], w, ys[N], ws=ws, stream=stream)
+        for _ in range(3):
+            chain()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(2000000)  # the host enqueues the chain before the start event fires
+        a.record(stream)
+        for _ in range(reps):
+            chain()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / reps * 1e3
+        flops = sum(2.0 * T * K * N for K, N, _ in layers)
+        out[f"T{T}"] = {"us_per_layer": round(us / len(layers), 2), "weight_gbs": round(wbytes / us / 1e3, 1),
+                        "hbm_frac": round(wbytes / us / 1e3 / hbm, 4), "tflops": round(flops / us / 1e6, 1),
+                        "tensor_frac": round(flops / us / 1e6 / tflops, 4)}
+        del xs, ys, ws
+    del layers
     return out
 
 
@@ -479,15 +524,15 @@ def run_e2e(args, c, vs, inp, d, dev, stream):
             "overlap": "host->device copy of step i+1 overlaps the kernels of step i (two device input sets)"}
 
 
-def oracle_sample(c, inp, topo_o, small=False):
-    """Times the float64 oracle on a bounded sample of one verify step and
-    extrapolates to the whole step by multiply-add counts.
+def oracle_sample(c, inp, topo_o, small=False, whole=False):
+    """Times the float64 oracle on one verify step.
 
-    Full sample: heads (all K heads), tree attention on layer 0 (x nl),
-    acceptance and packing in full, compaction on layer 0 (x nl).
-    Small sample: head 0 with the first V/8 vocabulary rows (scaled by MACs),
-    attention on layer 0 and the first 4 kv heads (x nl*Hkv/4), the rest as
-    above."""
+    whole: every call of the step in full (heads, packing, attention over all
+    layers, acceptance, compaction over all layers): nothing extrapolated.
+    Otherwise a bounded sample scaled to the step by multiply-add counts:
+    heads in full, tree attention on layer 0 (x nl), compaction on layer 0
+    (x nl); small: head 0 with the first V/8 vocabulary rows and attention on
+    layer 0 and the first 4 kv heads (x nl*Hkv/4)."""
     import oracle
     from oracle import topology as otopo
     K, H, V = c["K"], c["H"], c["V"]
@@ -506,21 +551,27 @@ def oracle_sample(c, inp, topo_o, small=False):
     t2 = time.perf_counter()
     G = c["Hq"] // c["Hkv"]
     nkv = 4 if small else c["Hkv"]
-    q = np.ascontiguousarray(inp["q"][:1, :, :, :nkv * G])
-    kc, vc = np.ascontiguousarray(inp["kc"][:1, :, :, :nkv]), np.ascontiguousarray(inp["vc"][:1, :, :, :nkv])
-    kt, vt = np.ascontiguousarray(inp["kt"][:1, :, :, :nkv]), np.ascontiguousarray(inp["vt"][:1, :, :, :nkv])
+    nl_s = c["nl"] if whole else 1
+    q = np.ascontiguousarray(inp["q"][:nl_s, :, :, :nkv * G])
+    kc, vc = np.ascontiguousarray(inp["kc"][:nl_s, :, :, :nkv]), np.ascontiguousarray(inp["vc"][:nl_s, :, :, :nkv])
+    kt, vt = np.ascontiguousarray(inp["kt"][:nl_s, :, :, :nkv]), np.ascontiguousarray(inp["vt"][:nl_s, :, :, :nkv])
     t2b = time.perf_counter()
     oracle.tree_attention(q, kc, vc, kt, vt, mask, inp["prefix_len"])
     t3 = time.perf_counter()
-    attn_scale = c["nl"] * c["Hkv"] / nkv
+    attn_scale = c["nl"] * c["Hkv"] / (nkv * nl_s)
     acc = oracle.typical_accept(inp["logits"], tokens, topo_o.parent, c["T"], c["eps"], c["delta"],
                                 Dmax=topo_o.max_depth)
     t4 = time.perf_counter()
-    oracle.kv_compact(inp["kc"][:1], inp["vc"][:1], inp["kt"][:1], inp["vt"][:1], acc["path_nodes"],
+    oracle.kv_compact(inp["kc"][:nl_s], inp["vc"][:nl_s], inp["kt"][:nl_s], inp["vt"][:nl_s], acc["path_nodes"],
                       acc["accept_len"], inp["prefix_len"])
     t5 = time.perf_counter()
-    step_s = (t1 - t0) * heads_scale + (t2 - t1) + (t3 - t2b) * attn_scale + (t4 - t3) + (t5 - t4) * c["nl"]
+    step_s = (t1 - t0) * heads_scale + (t2 - t1) + (t3 - t2b) * attn_scale + (t4 - t3) + (t5 - t4) * c["nl"] / nl_s
     work = (t1 - t0) + (t2 - t1) + (t3 - t2b) + (t4 - t3) + (t5 - t4)
+    if whole:
+        sample = (f"one whole verify step, nothing extrapolated: heads, tree packing, tree attention over all "
+                  f"{c['nl']} layers, typical acceptance, KV compaction over all layers; {work:.2f} s of CPU work, "
+                  f"single thread")
+        return step_s, sample, work
     if small:
         what = (f"head 0 on the first {V // 8} of {V} vocabulary rows (x{heads_scale:.1f} by MACs), "
                 f"tree attention on layer 0 x {nkv} of {c['Hkv']} kv heads (x{attn_scale:g})")
@@ -534,7 +585,7 @@ def oracle_sample(c, inp, topo_o, small=False):
 def cpu_baseline(c, inp, topo):
     from oracle import topology as otopo
     topo_o = otopo.greedy(otopo.synthetic_accuracy(c["K"], c["tree"][1]), c["tree"][2])
-    step_s, sample, _ = oracle_sample(c, inp, topo_o)
+    step_s, sample, _ = oracle_sample(c, inp, topo_o, whole=True)
     return {"value": round(1.0 / step_s, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
             "host_cpus": os.cpu_count()}
 
