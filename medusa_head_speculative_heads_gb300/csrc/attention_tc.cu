@@ -182,11 +182,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tma_prefetch(&tm_vc);
     tma_prefetch(&tm_kt);
     tma_prefetch(&tm_vt);
+    // The prefix cache is not written during a step: while an earlier kernel
+    // on the stream finishes, warm L2 with the first two K and V tiles of this
+    // CTA's first item (rows 0 .. 2 KT of its cache, whatever its length; the
+    // item's row and heads come from the launch alone).
+    if ((int)blockIdx.x < p.items) {
+      const int r = (int)blockIdx.x / p.mtiles;
+      const int lb = r / p.groups, h0 = p.packed ? 2 * (r % p.groups) : r % p.groups;
+      for (int t = 0; t < 2; ++t)
+        for (int kv = 0; kv < 2; ++kv)
+          for (int dh = 0; dh < 2; ++dh)
+            for (int cb = 0; cb < 2; ++cb)
+              tma_prefetch_l2_4d(kv ? &tm_vc : &tm_kc, 64 * dh, PACKED ? h0 + cb : h0,
+                                 PACKED ? t * p.KT : t * p.KT + 64 * cb, lb);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // Barriers, TMEM and descriptor prefetch above touch no global memory.
+  // Nothing above reads memory an earlier kernel may write.
   pdl_wait();
   pdl_trigger();
   const uint32_t tmem = s_tmem;

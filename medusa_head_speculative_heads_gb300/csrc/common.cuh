@@ -32,6 +32,9 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
 }
 
+// Hint: bring the 128-byte line holding p into L2 (no register, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // Two floats to packed bf16 (round to nearest even, hardware conversion); lo in
 // the low half.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {

@@ -181,6 +181,22 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
                   int n_counters, float* __restrict__ top_v, int* __restrict__ top_i) {
   extern __shared__ float xs[];  // [BB][C], then [BB][cap]
   __shared__ int s_last;
+  // Balanced contiguous row ranges: CTA, then warp (launch parameters only).
+  const int ctas = gridDim.x;
+  const int cap = (rows_per_head + ctas - 1) / ctas;
+  const int r_lo = (int)((long long)rows_per_head * blockIdx.x / ctas);
+  const int r_hi = (int)((long long)rows_per_head * (blockIdx.x + 1) / ctas);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = r_hi - r_lo;
+  const int w_lo = r_lo + n * warp / kGemvWarps;
+  const int w_hi = r_lo + n * (warp + 1) / kGemvWarps;
+  const TW* Wk = W + (size_t)blockIdx.y * rows_per_head * C;
+  // The weights are never written during a step: while an earlier kernel on
+  // the stream finishes, warm L2 with this warp's first row.
+  if (w_hi > w_lo) {
+    const char* row0 = reinterpret_cast<const char*>(Wk + (size_t)w_lo * C);
+    for (int off = lane * 128; off < C * (int)sizeof(TW); off += 32 * 128) prefetch_l2(row0 + off);
+  }
   pdl_wait();
   pdl_trigger();
   const int k = blockIdx.y;
@@ -197,17 +213,7 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
   }
   __syncthreads();
 
-  // Balanced contiguous row ranges: CTA, then warp.
-  const int ctas = gridDim.x;
-  const int cap = (rows_per_head + ctas - 1) / ctas;
   float* zs = xs + BB * C;
-  const int r_lo = (int)((long long)rows_per_head * blockIdx.x / ctas);
-  const int r_hi = (int)((long long)rows_per_head * (blockIdx.x + 1) / ctas);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = r_hi - r_lo;
-  const int w_lo = r_lo + n * warp / kGemvWarps;
-  const int w_hi = r_lo + n * (warp + 1) / kGemvWarps;
-  const TW* Wk = W + (size_t)k * rows_per_head * C;
 
   auto emit = [&](int row, int bb, float acc) {
     int b = b0 + bb;
