@@ -68,6 +68,8 @@ CASES = [
     (3, 2, 12, 1001, "f32", 0),   # scalar path
     (2, 3, 10, 1003, "bf16", 3),  # scalar path
     (4, 2, 3, 64, "f32", 0),      # S = 3: only head 1 has a position
+    (1, 3, 5, 1, "f32", 0),       # one-token vocabulary: p = 1, loss and gradient 0
+    (3, 2, 2, 50, "bf16", 0),     # S = 2: no head has a position
 ]
 
 
