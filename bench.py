@@ -503,10 +503,12 @@ def run_e2e(args, c, vs, inp, d, dev, stream):
     import torch
     from medusa_head_speculative_heads_gb300.step import PipelinedSteps
     names = PipelinedSteps.names
-    host = {k: _to_dev(inp[k], "cpu").pin_memory() for k in names}
     outs = [vs.accept_len, vs.path_nodes, vs.next_tok, vs.new_len]
     host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     pipe = PipelinedSteps(vs, {k: d[k] for k in names}, {k: d[k] for k in ("w1", "w2", "kc", "vc")}, outs, host_out)
+    host, views = pipe.host_staging()  # the step's inputs staged in one pinned buffer: one upload per step
+    for k in names:
+        views[k].copy_(_to_dev(inp[k], "cpu"))
     for _ in range(max(3, args.warmup)):
         pipe.step(host)
     pipe.reset()
@@ -521,7 +523,8 @@ def run_e2e(args, c, vs, inp, d, dev, stream):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": round(world / (ms / 1e3), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(pipe.bytes_h2d()), "d2h_bytes_per_step": int(pipe.bytes_d2h()),
-            "overlap": "host->device copy of step i+1 overlaps the kernels of step i (two device input sets)"}
+            "overlap": "host->device copy of step i+1 (one transfer of the step's staged inputs) overlaps the "
+                       "kernels of step i (two device input sets)"}
 
 
 def oracle_sample(c, inp, topo_o, small=False, whole=False):

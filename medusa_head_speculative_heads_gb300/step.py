@@ -131,23 +131,42 @@ class PipelinedSteps:
     inputs into the other set, which step i - 1 has finished reading.  Model
     state (weights, KV cache) stays resident and is shared by both sets.
 
+    Each device set is one buffer holding the inputs at fixed 256-byte aligned
+    offsets, so a step whose inputs are staged in the matching pinned host
+    buffer (`host_staging()`) is uploaded by a single copy: one large transfer
+    keeps the host link busier than seven of mixed sizes.  A dict of separate
+    pinned tensors is accepted too (one copy per tensor).
+
     `dev_inputs` maps the per-step input names (h, root_tok, prefix_len, q, kt,
-    vt, logits) to device tensors (set 0; set 1 is allocated alike);
-    `resident` holds w1, w2, kc, vc; `outs` are device results read back into
-    `host_outs` (pinned) at the end of every step."""
+    vt, logits) to device tensors (their shapes and dtypes define the layout;
+    their values fill both sets); `resident` holds w1, w2, kc, vc; `outs` are
+    device results read back into `host_outs` (pinned) at the end of every
+    step."""
 
     names = ("h", "root_tok", "prefix_len", "q", "kt", "vt", "logits")
 
     def __init__(self, vs: VerifyStep, dev_inputs: dict, resident: dict, outs, host_outs):
         import torch
         self.vs = vs
-        self.sets = [dict(dev_inputs), {k: torch.empty_like(dev_inputs[k]) for k in self.names}]
+        self.layout = []  # (name, offset, nbytes, dtype, shape)
+        off = 0
         for k in self.names:
-            self.sets[1][k].copy_(dev_inputs[k])
+            t = dev_inputs[k]
+            nb = t.numel() * t.element_size()
+            self.layout.append((k, off, nb, t.dtype, tuple(t.shape)))
+            off += (nb + 255) // 256 * 256
+        self.total = off
+        dev = dev_inputs[self.names[0]].device
+        self.bufs = [torch.empty(self.total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.sets = [self._views(b) for b in self.bufs]
+        for st in self.sets:
+            for k in self.names:
+                st[k].copy_(dev_inputs[k])
         self.outs, self.host_outs = list(outs), list(host_outs)
         self.copy_stream = torch.cuda.Stream()
         self.copied = [torch.cuda.Event(), torch.cuda.Event()]
         self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.last_h2d = 0
         r = resident
 
         def post():
@@ -158,15 +177,28 @@ class PipelinedSteps:
                                   s["kt"], s["vt"], s["logits"], post=post) for s in self.sets]
         self.i = 0
 
+    def _views(self, buf) -> dict:
+        return {k: buf[off:off + nb].view(dt).view(shape) for k, off, nb, dt, shape in self.layout}
+
+    def host_staging(self):
+        """A pinned host buffer in the device sets' layout and its per-input views
+        (fill the views, then pass the buffer to step())."""
+        import torch
+        hb = torch.empty(self.total, dtype=torch.uint8).pin_memory()
+        return hb, self._views(hb)
+
     def bytes_h2d(self) -> int:
-        return sum(self.sets[0][k].numel() * self.sets[0][k].element_size() for k in self.names)
+        """Bytes the last step copied host -> device (the inputs, plus alignment
+        padding when staged in one buffer)."""
+        return self.last_h2d or sum(nb for _, _, nb, _, _ in self.layout)
 
     def bytes_d2h(self) -> int:
         return sum(o.numel() * o.element_size() for o in self.outs)
 
-    def step(self, host_inputs: dict):
-        """Enqueues one step whose inputs are the pinned host tensors `host_inputs`
-        (no host synchronisation)."""
+    def step(self, host_inputs):
+        """Enqueues one step whose inputs are pinned host memory: the buffer from
+        host_staging() (one copy) or a dict of tensors (one copy each).  No host
+        synchronisation."""
         import torch
         s = self.i % 2
         main = torch.cuda.current_stream()
@@ -176,8 +208,15 @@ class PipelinedSteps:
         with torch.cuda.stream(cs):
             if self.i >= 2:
                 cs.wait_event(self.done[s])  # step i - 2 has finished reading this set
-            for k in self.names:
-                self.sets[s][k].copy_(host_inputs[k], non_blocking=True)
+            if isinstance(host_inputs, dict):
+                for k in self.names:
+                    self.sets[s][k].copy_(host_inputs[k], non_blocking=True)
+                self.last_h2d = sum(host_inputs[k].numel() * host_inputs[k].element_size() for k in self.names)
+            else:
+                if host_inputs.numel() != self.total or host_inputs.dtype != torch.uint8:
+                    raise ValueError("host buffer must come from host_staging()")
+                self.bufs[s].copy_(host_inputs, non_blocking=True)
+                self.last_h2d = self.total
             self.copied[s].record(cs)
         main.wait_event(self.copied[s])
         self.graphs[s].replay()

@@ -81,3 +81,41 @@ def test_pipelined_steps_match_sequential_steps(mg):
     np.testing.assert_array_equal(to_host(vs2.attn_out), ref["attn_out"])
     np.testing.assert_array_equal(to_host(kc2), ref["kc"])
     np.testing.assert_array_equal(to_host(vc2), ref["vc"])
+
+
+def test_pipelined_steps_from_one_staging_buffer(mg):
+    """The same steps staged in one pinned buffer per step (one upload each)."""
+    from medusa_head_speculative_heads_gb300.step import PipelinedSteps
+    c = wl.config("tiny")
+    steps = _steps(c, 3)
+    w1, w2 = to_dev(steps[0]["w1"]), to_dev(steps[0]["w2"])
+    vs = _verify_step(mg, c)
+    kc, vc = to_dev(steps[0]["kc"]), to_dev(steps[0]["vc"])
+    for inp in steps:
+        d = {k: to_dev(inp[k]) for k in PER_STEP}
+        vs.run(d["h"], w1, w2, d["root_tok"], d["prefix_len"], d["q"], kc, vc, d["kt"], d["vt"], d["logits"])
+    torch.cuda.synchronize()
+    vs2 = _verify_step(mg, c)
+    kc2, vc2 = to_dev(steps[0]["kc"]), to_dev(steps[0]["vc"])
+    outs = [vs2.accept_len, vs2.path_nodes, vs2.next_tok, vs2.new_len]
+    host_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    pipe = PipelinedSteps(vs2, {k: to_dev(steps[0][k]) for k in PER_STEP}, dict(w1=w1, w2=w2, kc=kc2, vc=vc2),
+                          outs, host_outs)
+    staged = []
+    for inp in steps:
+        hb, views = pipe.host_staging()
+        for k in PER_STEP:
+            views[k].copy_(torch.from_numpy(np.ascontiguousarray(inp[k])))
+        staged.append(hb)
+    pipe.reset()
+    for hb in staged:
+        pipe.step(hb)
+    torch.cuda.synchronize()
+    assert vs2.check() == 0
+    assert pipe.bytes_h2d() == staged[0].numel() >= sum(np.asarray(steps[0][k]).nbytes for k in PER_STEP)
+    np.testing.assert_array_equal(host_outs[0].numpy(), to_host(vs.accept_len))
+    np.testing.assert_array_equal(host_outs[1].numpy(), to_host(vs.path_nodes))
+    np.testing.assert_array_equal(host_outs[3].numpy(), to_host(vs.new_len))
+    np.testing.assert_array_equal(to_host(vs2.attn_out), to_host(vs.attn_out))
+    np.testing.assert_array_equal(to_host(kc2), to_host(kc))
+
