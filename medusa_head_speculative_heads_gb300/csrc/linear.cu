@@ -108,6 +108,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 0 && lane == 0) {
     tma_prefetch(&tm_w);
     tma_prefetch(&tm_x);
+    // The weights are not written while the layers of a pass run: while an
+    // earlier kernel on the stream finishes, bring this CTA's first ring's
+    // worth of weight boxes into L2 (x, an earlier layer's output, waits).
+    if ((int)blockIdx.x < p.units) {
+      const Unit x = decode(p, blockIdx.x);
+      const int kend = x.kb1 < x.kb0 + p.stages ? x.kb1 : x.kb0 + p.stages;
+      for (int kb = x.kb0; kb < kend; ++kb) tma_prefetch_l2_2d(&tm_w, kb * 64, x.mt * 128);
+    }
   }
   tc_fence_before();
   __syncthreads();
