@@ -77,12 +77,15 @@ __global__ void __launch_bounds__(kPartThreads)
 node_partial_kernel(const float* __restrict__ logits, int N, int V, int C, float T, float4* __restrict__ part) {
   __shared__ float sv[kPartThreads / 32];
   __shared__ int si[kPartThreads / 32];
-  pdl_wait();
-  pdl_trigger();
   const int c = blockIdx.x, n = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const float* z = logits + ((size_t)b * N + n) * V;
   const int cs = ((V + C - 1) / C + 3) & ~3;  // chunk size, a multiple of 4
   const int lo = c * cs, hi = min(V, lo + cs);
+  // While an earlier kernel on the stream finishes, bring this chunk into L2
+  // (a hint: L2 is where every write lands, so nothing stale can be read).
+  for (int v = lo + tid * 32; v < hi; v += kPartThreads * 32) prefetch_l2(z + v);
+  pdl_wait();
+  pdl_trigger();
   const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
 
   float mv = -INFINITY;
