@@ -10,20 +10,38 @@
 // Kernel 1 moves 16-byte (or 4-byte) words: one thread per word of every
 // (layer, row, path slot, kv head) row; slots past accept_len do nothing.
 // Kernel 2 writes new_len after kernel 1 has read prefix_len, so new_len may
-// alias prefix_len.
+// alias prefix_len; when it does not, kernel 1's first B threads write it
+// and kernel 2 is not launched.
 #include "common.cuh"
 #include "host_util.h"
 
 namespace medusa {
+
+// new_len of row b: prefix_len + accept_len when the row is valid (accept
+// length in range, fits the cache, every path node in range), else unchanged.
+__device__ __forceinline__ int kv_new_len(const int32_t* prefix_len, const int32_t* accept_len,
+                                          const int32_t* path_nodes, int b, int Lmax, int Dmax, int N) {
+  const int L = prefix_len[b], A = accept_len[b];
+  bool ok = A >= 1 && A <= Dmax + 1 && L >= 0 && L + A <= Lmax;
+  for (int j = 0; ok && j < A; ++j) {
+    const int nj = path_nodes[(size_t)b * (Dmax + 1) + j];
+    ok = nj >= 0 && nj < N;
+  }
+  return ok ? L + A : L;
+}
 
 template <typename WORD>
 __global__ void kv_gather_kernel(WORD* __restrict__ kc, WORD* __restrict__ vc, const WORD* __restrict__ kt,
                                  const WORD* __restrict__ vt, const int32_t* __restrict__ path_nodes,
                                  const int32_t* __restrict__ accept_len, const int32_t* __restrict__ prefix_len,
                                  int nl, int B, int N, int Lmax, int Dmax, int words_per_row,
-                                 long long total, int32_t* d_status) {
+                                 long long total, int32_t* d_status, int32_t* __restrict__ new_len_separate) {
   pdl_wait();
   pdl_trigger();
+  if (new_len_separate) {  // does not alias prefix_len: written here, no second kernel
+    const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (b < B) new_len_separate[b] = kv_new_len(prefix_len, accept_len, path_nodes, (int)b, Lmax, Dmax, N);
+  }
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
        t += (long long)gridDim.x * blockDim.x) {
     // t = (((l * B + b) * (Dmax+1) + i) * words_per_row + w) * 2 + kv
@@ -68,13 +86,7 @@ __global__ void kv_len_kernel(const int32_t* prefix_len, const int32_t* accept_l
   pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
-  const int L = prefix_len[b], A = accept_len[b];
-  bool ok = A >= 1 && A <= Dmax + 1 && L >= 0 && L + A <= Lmax;
-  for (int j = 0; ok && j < A; ++j) {
-    const int nj = path_nodes[(size_t)b * (Dmax + 1) + j];
-    ok = nj >= 0 && nj < N;
-  }
-  new_len[b] = ok ? L + A : L;
+  new_len[b] = kv_new_len(prefix_len, accept_len, path_nodes, b, Lmax, Dmax, N);
 }
 
 }  // namespace medusa
@@ -109,18 +121,22 @@ extern "C" medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, c
   long long blocks = (total + threads - 1) / threads;
   const long long cap = (long long)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
+  // One kernel when new_len is a separate buffer the grid's first B threads can write.
+  const bool fused = !overlaps(new_len, (size_t)B * 4, prefix_len, (size_t)B * 4) && blocks * threads >= B;
+  int32_t* nl_sep = fused ? new_len : nullptr;
   if (v16)
     launch_pdl(kv_gather_kernel<uint4>, dim3((int)blocks), dim3(threads), 0, s, (uint4*)kc, (uint4*)vc, (const uint4*)kt,
                                                            (const uint4*)vt, path_nodes, accept_len,
                                                            prefix_len, n_layers, B, N, Lmax, Dmax,
-                                                           wpr, total, d_status);
+                                                           wpr, total, d_status, nl_sep);
   else
     launch_pdl(kv_gather_kernel<uint32_t>, dim3((int)blocks), dim3(threads), 0, s, (uint32_t*)kc, (uint32_t*)vc,
                                                                (const uint32_t*)kt, (const uint32_t*)vt,
                                                                path_nodes, accept_len, prefix_len,
                                                                n_layers, B, N, Lmax, Dmax, wpr, total,
-                                                               d_status);
-  launch_pdl(kv_len_kernel, dim3((B + 127) / 128), dim3(128), 0, s, prefix_len, accept_len, new_len, B, Lmax, Dmax,
-                                                path_nodes, N);
+                                                               d_status, nl_sep);
+  if (!fused)
+    launch_pdl(kv_len_kernel, dim3((B + 127) / 128), dim3(128), 0, s, prefix_len, accept_len, new_len, B, Lmax,
+               Dmax, path_nodes, N);
   return launch_status();
 }

@@ -115,7 +115,7 @@ class VerifyStep:
         else:
             heads = 2 * (-(-B // 8))  # W1 and W2 per pass of <= 8 rows; the W2 pass merges the top-k
         attn = self.attn_launches
-        return heads + 1 + attn + 2 + 2
+        return heads + 1 + attn + 2 + 1  # compaction: one kernel (new_len is a buffer of its own)
 
     def check(self, stream=None) -> int:
         return B_.medusa_status_check(self.status, stream)
