@@ -166,7 +166,9 @@ medusa_status medusa_head_topk(const float* logits, int rows, int V, int topk, i
  *   tokens[b][0] = root_tok[b];  tokens[b][n] = topk_idx[b][depth(n)-1][rank(n)]
  *   pos[b][n]    = prefix_len[b] + depth(n)
  *   mask[n][w]   bit (j % 32) of word j / 32 set iff node j is n or an ancestor
- *                of n (batch-independent, ceil(N/32) words per node)
+ *                of n (batch-independent, ceil(N/32) words per node); mask may be
+ *                NULL: it depends on the topology alone, so a caller that holds it
+ *                for this topology can skip it (the topology checks still run)
  *   root_tok [B], prefix_len [B], tokens [B][N], pos [B][N]: int32;
  *   topk_idx [B][K][topk] from medusa_heads.  Needs topology max_depth <= K and
  *   max_rank <= topk (INVALID_ARG otherwise).  A rank or parent that the device

@@ -257,6 +257,8 @@ def medusa_tree_build(topo: DevTopology, root_tok, topk_idx, prefix_len, tokens=
         pos = torch.empty((B, N), dtype=torch.int32, device=dev)
     if mask is None:
         mask = torch.empty((N, (N + 31) // 32), dtype=torch.int32, device=dev)
+    elif mask is False:  # the mask depends on the topology alone: not written
+        mask = None
     _check("medusa_tree_build", lib().medusa_tree_build(
         ctypes.byref(topo.st), _ptr(root_tok), _ptr(topk_idx), B, K, topk, _ptr(prefix_len), _ptr(tokens),
         _ptr(pos), _ptr(mask), _ptr(d_status), _stream(stream)))

@@ -78,7 +78,7 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
     }
 #pragma unroll
     for (int w = 0; w < kMaskWords; ++w)
-      if (w < W) mask[(size_t)n * W + w] = row[w];
+      if (w < W && mask) mask[(size_t)n * W + w] = row[w];
   }
 }
 
@@ -91,7 +91,7 @@ extern "C" medusa_status medusa_tree_build(const medusa_dev_topology* t, const i
                                            const int32_t* prefix_len, int32_t* tokens, int32_t* pos,
                                            uint32_t* mask, int32_t* d_status,
                                            medusa_stream_t stream) {
-  if (!t || !root_tok || !topk_idx || !prefix_len || !tokens || !pos || !mask) return MEDUSA_ERR_INVALID_ARG;
+  if (!t || !root_tok || !topk_idx || !prefix_len || !tokens || !pos) return MEDUSA_ERR_INVALID_ARG;
   if (!t->parent || !t->depth || !t->rank) return MEDUSA_ERR_INVALID_ARG;
   if (B < 1 || K < 1 || K > MEDUSA_MAX_DEPTH || topk < 1 || topk > MEDUSA_MAX_TOPK) return MEDUSA_ERR_INVALID_ARG;
   if (t->n_nodes < 1 || t->n_nodes > MEDUSA_MAX_NODES) return MEDUSA_ERR_INVALID_ARG;

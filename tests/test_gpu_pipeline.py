@@ -119,3 +119,21 @@ def test_pipelined_steps_from_one_staging_buffer(mg):
     np.testing.assert_array_equal(to_host(vs2.attn_out), to_host(vs.attn_out))
     np.testing.assert_array_equal(to_host(kc2), to_host(kc))
 
+
+
+def test_tree_build_without_mask(mg):
+    """The mask depends on the topology alone: packing without it writes the same
+    tokens and positions (what a step that holds the mask runs every step)."""
+    c = wl.config("tiny")
+    dt = lib_topology(mg, c).upload()
+    B, K, topk = 2, c["K"], c["topk"]
+    rng = np.random.default_rng(4)
+    root = to_dev(rng.integers(0, c["V"], B).astype(np.int32))
+    idx = to_dev(rng.integers(0, c["V"], (B, K, topk)).astype(np.int32))
+    pl = to_dev(np.array([9, 40], np.int32))
+    t1, p1, m1 = mg.medusa_tree_build(dt, root, idx, pl)
+    t2, p2, m2 = mg.medusa_tree_build(dt, root, idx, pl, mask=False)
+    torch.cuda.synchronize()
+    assert m2 is None
+    np.testing.assert_array_equal(to_host(t1), to_host(t2))
+    np.testing.assert_array_equal(to_host(p1), to_host(p2))
