@@ -51,8 +51,11 @@ def test_noalloc_accept_rejects_sizes_beyond_its_array():
     mg.build()
     t = otopo.dense([4, 4, 4, 4], 256)
     dt = mg.Topology.dense([4, 4, 4, 4], 256).upload()
-    B, V = 32, 32000  # 32 * 256 * 16 chunks * 16 B = 2 MiB > 1 MiB
-    # rejected before any launch, so stride-0 views of one element stand in for the inputs
+    B, V = 256, 32000  # 256 rows x 256 nodes x (8 to 32 chunks) x 16 B = 8 to 32 MiB > 1 MiB
+    # Stride-0 views of one element stand in for the inputs, which is safe only
+    # because the call is rejected before any launch: check the library's own
+    # size rule first, so this test can never launch on them.
+    assert mg.lib().medusa_typical_accept_workspace_size(B, t.n_nodes, V) > (1 << 20)
     logits = torch.zeros(1, dtype=torch.float32, device="cuda").expand(B, t.n_nodes, V)
     tokens = torch.zeros(1, dtype=torch.int32, device="cuda").expand(B, t.n_nodes)
     with pytest.raises(mg.MedusaError) as e:
