@@ -205,11 +205,43 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
     if (b0 == 0 && blockIdx.x == 0 && blockIdx.y == 0)
       for (int i = threadIdx.x; i < n_counters; i += kGemvThreads) counters[i] = 0;
   }
-  for (int idx = threadIdx.x; idx < BB * C; idx += kGemvThreads) {
-    int bb = idx / C, c = idx - bb * C, b = b0 + bb;
-    float v = 0.f;
-    if (b < B) v = kFirst ? load_elem<TW>(h, (size_t)b * C + c) : u[((size_t)b * K + k) * C + c];
-    xs[idx] = v;
+  // Stage the vector(s) in shared memory: 16-byte loads, four per thread issued
+  // before the first store (one round trip, not one per element), rows past B
+  // as zeros; element by element when the rows are not 16-byte aligned.
+  constexpr int XV = kFirst ? Vec16<TW>::n : 4;  // elements per 16-byte chunk
+  const void* x_base = kFirst ? static_cast<const void*>(h) : static_cast<const void*>(u);
+  if (C % XV == 0 && (reinterpret_cast<uintptr_t>(x_base) & 15u) == 0) {
+    constexpr int XU = 4;
+    const int per_row = C / XV, nch = BB * per_row;
+    for (int i0 = threadIdx.x; i0 < nch; i0 += kGemvThreads * XU) {
+      uint4 raw[XU];
+#pragma unroll
+      for (int j = 0; j < XU; ++j) {
+        const int i = i0 + j * kGemvThreads, bb = i / per_row, cc = i - bb * per_row, b = b0 + bb;
+        raw[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < nch && b < B)
+          raw[j] = kFirst ? *reinterpret_cast<const uint4*>(h + (size_t)b * C + (size_t)cc * XV)
+                          : *reinterpret_cast<const uint4*>(u + ((size_t)b * K + k) * C + (size_t)cc * XV);
+      }
+#pragma unroll
+      for (int j = 0; j < XU; ++j) {
+        const int i = i0 + j * kGemvThreads;
+        if (i >= nch) break;
+        float f[XV];
+        if constexpr (XV == 8) unpack_bf16x8(raw[j], f);
+        else unpack_f32x4(raw[j], f);
+        float4* dst = reinterpret_cast<float4*>(xs + (size_t)i * XV);
+#pragma unroll
+        for (int e = 0; e < XV / 4; ++e) dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+      }
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < BB * C; idx += kGemvThreads) {
+      int bb = idx / C, c = idx - bb * C, b = b0 + bb;
+      float v = 0.f;
+      if (b < B) v = kFirst ? load_elem<TW>(h, (size_t)b * C + c) : u[((size_t)b * K + k) * C + c];
+      xs[idx] = v;
+    }
   }
   __syncthreads();
 
