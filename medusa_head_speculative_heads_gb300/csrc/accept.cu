@@ -179,6 +179,8 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   pdl_wait();
   pdl_trigger();
   if (tid == 0) s_bad = 0;
+  // the topology of node c, loaded with the partials below (one round trip)
+  const int dc_ld = c < N ? depth[c] : -1, pc_ld = c < N ? parent[c] : -1;
   // 1. statistics of every node: grp threads per node, strided over the chunks
   {
     const int node = tid / grp, sub = tid % grp;
@@ -218,8 +220,8 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   __syncthreads();
   int dc = -1, pc = -1;
   if (c < N) {
-    dc = depth[c];
-    pc = parent[c];
+    dc = dc_ld;
+    pc = pc_ld;
     if (c > 0 && (pc < 0 || pc >= c || dc < 1 || dc > max_depth)) s_bad = 1;
     acc[c] = c == 0 ? 1 : 0;
     par[c] = pc;

@@ -313,9 +313,28 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
           const int b = b0 + bb;
           if (b >= B) continue;
           const size_t base = ((size_t)b * K + k) * ctas * topk;
-          for (int i = threadIdx.x; i < ctas * topk; i += kGemvThreads) {
-            mv[bb * ctas * topk + i] = __ldcg(cand_v + base + i);
-            mi[bb * ctas * topk + i] = __ldcg(cand_i + base + i);
+          // every load of a thread in flight before its first store (one round trip)
+          constexpr int MU = 8;
+          const int n = ctas * topk;
+          for (int i0 = threadIdx.x; i0 < n; i0 += kGemvThreads * MU) {
+            float cv[MU];
+            int ci[MU];
+#pragma unroll
+            for (int j = 0; j < MU; ++j) {
+              const int i = i0 + j * kGemvThreads;
+              if (i < n) {
+                cv[j] = __ldcg(cand_v + base + i);
+                ci[j] = __ldcg(cand_i + base + i);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < MU; ++j) {
+              const int i = i0 + j * kGemvThreads;
+              if (i < n) {
+                mv[bb * n + i] = cv[j];
+                mi[bb * n + i] = ci[j];
+              }
+            }
           }
         }
         __syncthreads();
