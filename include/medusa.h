@@ -298,7 +298,7 @@ medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, const void* 
 medusa_status medusa_tree_rope(void* q, void* k, const int32_t* pos, int n_layers, int B, int N, int Hq,
                                int Hkv, int d, float base, medusa_dtype dt, medusa_stream_t stream);
 
-/* --------------------------------------------------------------- (f2) linear
+/* ---------------------------------------------------------------- (g) linear
  * One linear layer of the verify pass over the tree tokens (paper review,
  * roofline in "实验设计与结果" and "局限性": verifying N candidates runs every
  * linear layer of the backbone over B * N tokens, which lifts decoding's
@@ -315,7 +315,7 @@ size_t medusa_linear_workspace_size(int T, int K, int Nout);
 medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
                             void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
 
-/* ------------------------------------------------ (f3) online tree calibration
+/* ------------------------------------------------- (h) online tree calibration
  * The sparse tree of the paper review ("方法细节") is built from per-head top-i
  * accuracies measured on calibration data; these calls measure them on the
  * verify steps and rebuild the tree on the device.
@@ -357,7 +357,7 @@ medusa_status medusa_topology_greedy_device(const double* acc, int K, int R, int
                                             size_t buf_elems, int32_t* d_meta, medusa_dev_topology* out,
                                             int32_t* d_status, medusa_stream_t stream);
 
-/* ------------------------------------------------------------ (f4) head loss
+/* ------------------------------------------------------------- (i) head loss
  * The Medusa-1 training loss of the K heads and its gradient with respect to
  * the head logits, in one call (paper review, "方法细节": the backbone is
  * frozen and only the heads train, on L1 = -sum_{k=1..K} lambda_k
