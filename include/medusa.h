@@ -315,6 +315,15 @@ size_t medusa_linear_workspace_size(int T, int K, int Nout);
 medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
                             void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
 
+/* medusa_linear_test_stall: failure-detection test hook.  Runs medusa_linear
+ * (bf16) with the first stage's loads withheld, so the kernel's bounded
+ * barrier waits (1 s) expire: the kernel stops every role, drains its copies
+ * and MMAs, frees its tensor memory and sets MEDUSA_DEV_TIMEOUT in d_status;
+ * y is not meaningful.  The call leaves the context usable (no fault, no
+ * trap).  Same arguments and validation as medusa_linear. */
+medusa_status medusa_linear_test_stall(const void* x, const void* w, void* y, int T, int K, int Nout, void* ws,
+                                       size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
+
 /* ------------------------------------------------- (h) online tree calibration
  * The sparse tree of the paper review ("方法细节") is built from per-head top-i
  * accuracies measured on calibration data; these calls measure them on the

@@ -30,7 +30,7 @@ EXPORTS = (
     "medusa_typical_accept_workspace_size", "medusa_typical_accept", "medusa_kv_compact",
     "medusa_status_check", "medusa_status_string", "medusa_version", "medusa_typical_accept_noalloc",
     "medusa_tree_rope", "medusa_accept_stats", "medusa_acc_update", "medusa_topology_greedy_device_elems",
-    "medusa_topology_greedy_device", "medusa_linear_workspace_size", "medusa_linear",
+    "medusa_topology_greedy_device", "medusa_linear_workspace_size", "medusa_linear", "medusa_linear_test_stall",
     "medusa_head_loss_workspace_size", "medusa_head_loss",
 )
 
@@ -93,6 +93,7 @@ def lib():
             "medusa_accept_stats": (I, [P, P, P, I, I, I, P, P, P, P]),
             "medusa_linear_workspace_size": (Z, [I, I, I]),
             "medusa_linear": (I, [P, P, P, I, I, I, I, P, Z, P, P]),
+            "medusa_linear_test_stall": (I, [P, P, P, I, I, I, P, Z, P, P]),
             "medusa_head_loss_workspace_size": (Z, [I, I, I]),
             "medusa_head_loss": (I, [P, P, I, I, I, I, ctypes.c_float, I, P, P, P, P, Z, P, P]),
             "medusa_acc_update": (I, [P, P, P, I, I, ctypes.c_double, P]),
@@ -404,6 +405,18 @@ def medusa_head_loss(logits, tokens, decay: float = 0.8, grad: bool = True, dlog
         _ptr(logits), _ptr(tokens), K, B, S, V, float(decay), _dtype_code(logits), _ptr(dlogits), _ptr(loss),
         _ptr(row_loss), _ptr(ws), 0 if ws is None else ws.numel(), _ptr(d_status), _stream(stream)))
     return loss, dlogits
+
+
+def medusa_linear_test_stall(x, w, y, d_status, ws=None, stream=None):
+    """Failure-detection test hook: medusa_linear with its first loads withheld, so
+    the kernel's bounded waits expire and d_status becomes MEDUSA_DEV_TIMEOUT."""
+    T, K = x.shape
+    Nout = w.shape[0]
+    ws = _ws(lib().medusa_linear_workspace_size(T, K, Nout), x.device, ws)
+    _check("medusa_linear_test_stall", lib().medusa_linear_test_stall(
+        _ptr(x), _ptr(w), _ptr(y), T, K, Nout, _ptr(ws), 0 if ws is None else ws.numel(), _ptr(d_status),
+        _stream(stream)))
+    return y
 
 
 def medusa_accept_stats(path_nodes, accept_len, topo: DevTopology, R: int, tested, accepted, d_status=None,

@@ -518,12 +518,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (alive && pend) alive = finish();
   }
 
-  if (threadIdx.x == 0 || (warp == 1 && lane == 0) || (warp == 2 && lane == 0) || (warp == 4 && lane == 0)) {
-    if (s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // After the barrier: any role's timeout (even one raised after another role
+  // finished) is visible here.
+  if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 

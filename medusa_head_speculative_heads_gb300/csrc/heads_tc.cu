@@ -220,10 +220,12 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
   }
 
-  if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // After the barrier: any role's timeout (even one raised after another role
+  // finished) is visible here.
+  if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 

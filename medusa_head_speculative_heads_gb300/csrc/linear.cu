@@ -45,6 +45,7 @@ constexpr uint64_t kDrainNs = 100000000ull;
 
 struct Params {
   int T, K, Nout, TN, mtiles, ntiles, S, kblocks, units, stages;
+  int withhold_first;  // test hook: the first stage's loads are never issued
   uint32_t stage_bytes;
   uint16_t* y;
   float* part;       // [tiles][S][TN][128] when S > 1 (feature fastest: coalesced)
@@ -139,6 +140,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             break;
           uint8_t* st = smem + s * p.stage_bytes;
           mbar_expect_tx(&bars->full[s], kATile + b_bytes);
+          if (p.withhold_first && g == 0) continue;  // that stage never fills: the bounded waits expire
           tma_load_2d(st, &tm_w, &bars->full[s], kb * 64, x.mt * 128);
           tma_load_2d(st + kATile, &tm_x, &bars->full[s], kb * 64, x.nt * p.TN);
         }
@@ -217,10 +219,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     }
   }
 
-  if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // After the barrier: any role's timeout (even one raised after another role
+  // finished) is visible here.
+  if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -346,8 +350,9 @@ extern "C" size_t medusa_linear_workspace_size(int T, int K, int Nout) {
   return L.part_bytes;
 }
 
-extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
-                                       void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream) {
+static medusa_status linear_call(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
+                                 void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream,
+                                 int withhold_first) {
   if (!x || !w || !y || T < 1 || K < 8 || Nout < 1) return MEDUSA_ERR_INVALID_ARG;
   if (dt != MEDUSA_BF16) return MEDUSA_ERR_UNSUPPORTED;
   if (K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(y)) return MEDUSA_ERR_INVALID_ARG;
@@ -375,6 +380,7 @@ extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, in
   p.y = static_cast<uint16_t*>(y);
   p.part = L.S > 1 ? static_cast<float*>(ws) : nullptr;
   p.d_status = d_status;
+  p.withhold_first = withhold_first;
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lin::kSmemBytes) !=
       cudaSuccess)
     return MEDUSA_ERR_CUDA;
@@ -386,3 +392,15 @@ extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, in
   }
   return launch_status();
 }
+
+extern "C" medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
+                                       void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream) {
+  return linear_call(x, w, y, T, K, Nout, dt, ws, ws_bytes, d_status, stream, 0);
+}
+
+extern "C" medusa_status medusa_linear_test_stall(const void* x, const void* w, void* y, int T, int K, int Nout,
+                                                  void* ws, size_t ws_bytes, int32_t* d_status,
+                                                  medusa_stream_t stream) {
+  return linear_call(x, w, y, T, K, Nout, MEDUSA_BF16, ws, ws_bytes, d_status, stream, 1);
+}
+
