@@ -7,6 +7,7 @@
 // sparse tree construction).  A node is its rank path (element j = rank within
 // Medusa head j+1's top-k).  Canonical order sorts paths by (length,
 // lexicographic), so the root is node 0 and parents precede children.
+#include <atomic>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -70,18 +71,19 @@ static medusa_status fill_topology(const std::vector<Path>& paths, medusa_topolo
   return MEDUSA_OK;
 }
 
-static int cached_sm_count[64] = {0};
+// Per-device cache; concurrent first calls may both query, and store the same value.
+static std::atomic<int> cached_sm_count[64];
 
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kNumSMsFallback;
-  if (!cached_sm_count[dev]) {
-    int n = 0;
+  int n = cached_sm_count[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = kNumSMsFallback;
-    cached_sm_count[dev] = n;
+    cached_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return cached_sm_count[dev];
+  return n;
 }
 
 }  // namespace medusa
