@@ -289,6 +289,23 @@ def run_ours(args, c):
         dist.destroy_process_group()
 
 
+def _capture(fn):
+    """fn(s) (stream-ordered calls on stream s) captured into a CUDA graph on a
+    side stream, after one eager run there outside capture; replay() launches
+    it on the current stream."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn(s)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
 def time_calibration(mg, vs, c, N, K, stream, dev):
     """Online tree calibration calls (outside the five-call step): this step's
     acceptance statistics, the accuracy-table update and a device rebuild of the
@@ -300,22 +317,26 @@ def time_calibration(mg, vs, c, N, K, stream, dev):
     accepted = torch.zeros_like(tested)
     acc = torch.tensor(wl.synthetic_accuracy(c["K"], c["tree"][1]), dtype=torch.float64, device=dev)
     calls = {
-        "accept_stats": lambda: mg.medusa_accept_stats(vs.path_nodes, vs.accept_len, vs.topo, R, tested, accepted,
-                                                       stream=stream),
-        "acc_update": lambda: mg.medusa_acc_update(acc[:Dmax], tested, accepted, 64.0, stream=stream),
-        "greedy_rebuild": lambda: mg.medusa_topology_greedy_device(acc, N, stream=stream),
+        "accept_stats": lambda s: mg.medusa_accept_stats(vs.path_nodes, vs.accept_len, vs.topo, R, tested, accepted,
+                                                         stream=s),
+        "acc_update": lambda s: mg.medusa_acc_update(acc[:Dmax], tested, accepted, 64.0, stream=s),
+        "greedy_rebuild": lambda s: mg.medusa_topology_greedy_device(acc, N, stream=s),
     }
     out = {}
     for name, fn in calls.items():
         for _ in range(3):
-            fn()
+            fn(stream)
+        # K calls in one CUDA graph: the host's per-call cost (binding, launch)
+        # stays out of the device time of these few-microsecond kernels.
+        g = _capture(lambda s: [fn(s) for _ in range(K)])
+        g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(K):
-            fn()
+        g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         out[name + "_us"] = round(e0.elapsed_time(e1) / K * 1e3, 2)
+        del g
     out["tree"] = f"{N} nodes from a {c['K']} x {c['tree'][1]} accuracy table"
     return out
 
@@ -396,16 +417,20 @@ def time_linear_chain(mg, c, stream, dev, reps=10):
         ws = torch.empty(max(1, max(mg.lib().medusa_linear_workspace_size(T, K, N) for K, N in shapes)),
                          dtype=torch.uint8, device=dev)
 
-        def chain():
+        def chain(s):
             for K, N, w in layers:
-                mg.medusa_linear(xs[K], w, ys[N], ws=ws, stream=stream)
+                mg.medusa_linear(xs[K], w, ys[N], ws=ws, stream=s)
         for _ in range(3):
-            chain()
+            chain(stream)
+        # the 8 calls (up to 16 launches) as one CUDA graph, replayed back to
+        # back: device time only, the host's per-call cost is not on the path
+        gr = _capture(chain)
+        for _ in range(3):
+            gr.replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(2000000)  # the host enqueues the chain before the start event fires
         a.record(stream)
         for _ in range(reps):
-            chain()
+            gr.replay()
         b.record(stream)
         torch.cuda.synchronize()
         us = a.elapsed_time(b) / reps * 1e3
@@ -413,7 +438,7 @@ def time_linear_chain(mg, c, stream, dev, reps=10):
         out[f"T{T}"] = {"us_per_layer": round(us / len(layers), 2), "weight_gbs": round(wbytes / us / 1e3, 1),
                         "hbm_frac": round(wbytes / us / 1e3 / hbm, 4), "tflops": round(flops / us / 1e6, 1),
                         "tensor_frac": round(flops / us / 1e6 / tflops, 4)}
-        del xs, ys, ws
+        del gr, xs, ys, ws
     del layers
     return out
 

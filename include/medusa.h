@@ -307,10 +307,11 @@ medusa_status medusa_tree_rope(void* q, void* k, const int32_t* pos, int n_layer
  *   x [T][K] (T = B * N tokens), W [Nout][K] (row-major (out, in)), y [T][Nout];
  *   bf16 only (UNSUPPORTED otherwise), fp32 accumulation, y rounded once to
  *   bf16.  K % 8 == 0, pointers 16-byte aligned; y must not overlap x or W
- *   (ALIAS).  When the output tiles are too few to occupy the GPU, the K range
- *   is split and the partials are added in a fixed order (deterministic);
- *   the scratch for that is medusa_linear_workspace_size(T, K, Nout) bytes
- *   (for the current device; 0 = none needed), 16-byte aligned. */
+ *   (ALIAS).  The K blocks of all output tiles are divided evenly over the
+ *   SMs; a tile whose K range two or more CTAs share is summed from their
+ *   fp32 partials in a fixed order (deterministic on a given device); the
+ *   scratch for those is medusa_linear_workspace_size(T, K, Nout) bytes (for
+ *   the current device; 0 = none needed), 16-byte aligned. */
 size_t medusa_linear_workspace_size(int T, int K, int Nout);
 medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
                             void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);

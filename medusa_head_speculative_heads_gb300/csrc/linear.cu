@@ -10,15 +10,21 @@
 // (row-major, the usual (out, in) layout), y [T][Nout].
 //
 // Tiles of 128 output features (the weight rows, MMA M = 128) by up to 256
-// tokens (MMA N = TN).  Few tiles (small T, narrow layers) would leave SMs idle
-// while the weights stream from HBM, so each tile's K range is split S ways
-// into fp32 partials, which a second kernel adds in a fixed order (four
-// output features per thread; deterministic).  Roles (256 threads, persistent
-// over the units): warp 0 lane 0 issues TMA loads of the W and x boxes
-// (128-byte swizzle) into a 4- to 12-stage ring (216 KB); warp 1 owns TMEM and lane 0 issues the MMAs into one of
-// two 256-column accumulators; warps 4-7 read the accumulator 32 columns at a
-// time (one feature row per thread) and write y or the partial.  Every wait is
-// bounded; a timeout sets MEDUSA_DEV_TIMEOUT, drains and frees TMEM.
+// tokens (MMA N = TN).  The K blocks of all tiles, laid end to end tile after
+// tile, are divided evenly over the grid (one CTA per SM): CTA c takes the
+// contiguous range [c W / G, (c + 1) W / G) of the W = tiles x K-block
+// sequence, so no SM idles when the tile count is not a multiple of the SM
+// count (a small T or narrow layer has fewer tiles than SMs; 172 tiles of a
+// 22016-wide layer would otherwise take two rounds on 152 SMs).  A tile whose
+// K range a CTA covers whole is written to y by that CTA; a tile shared by
+// several CTAs (at most the first and the last of each CTA's range) leaves an
+// fp32 partial per CTA, which a second kernel adds in CTA order (a fixed
+// order: deterministic).  Roles (256 threads): warp 0 lane 0 issues TMA loads
+// of the W and x boxes (128-byte swizzle) into a 4- to 14-stage ring (216 KB);
+// warp 1 owns TMEM and lane 0 issues the MMAs into one of two 256-column
+// accumulators; warps 4-7 read the accumulator 32 columns at a time (one
+// feature row per thread) and write y or the partial.  Every wait is bounded;
+// a timeout sets MEDUSA_DEV_TIMEOUT, drains and frees TMEM.
 #include <cuda.h>
 #include <math.h>
 #include <cudaTypedefs.h>
@@ -34,7 +40,8 @@ namespace lin {
 
 constexpr int kThreads = 256;
 constexpr int kMaxStages = 14;
-constexpr int kMaxSplit = 16;
+constexpr int kMinBlocksPerCta = 4;       // K blocks: fewer CTAs when the whole product is smaller
+constexpr int kReduceCols = 16;           // token columns per block of the partial reduction
 constexpr uint32_t kATile = 16384;        // 128 W rows x 128 bytes
 constexpr uint32_t kRingBytes = 221184;   // 216 KB of stages
 constexpr uint32_t kBarBytes = 512;
@@ -44,11 +51,12 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
 struct Params {
-  int T, K, Nout, TN, mtiles, ntiles, S, kblocks, units, stages;
+  int T, K, Nout, TN, mtiles, ntiles, kblocks, grid, stages;
+  long long work;      // tiles x kblocks, divided evenly over the grid
   int withhold_first;  // test hook: the first stage's loads are never issued
   uint32_t stage_bytes;
   uint16_t* y;
-  float* part;       // [tiles][S][TN][128] when S > 1 (feature fastest: coalesced)
+  float* part;       // [grid][2][TN][128] when some tile is shared (feature fastest: coalesced)
   int32_t* d_status;
 };
 
@@ -62,18 +70,33 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-struct Unit {
-  int tile, mt, nt, s, kb0, kb1;
+// First flattened K block of CTA c (tile-major: block w is K block w % kblocks
+// of tile w / kblocks); CTA c owns [work_begin(c), work_begin(c + 1)).
+__host__ __device__ __forceinline__ long long work_begin(long long work, int grid, int c) {
+  return work * c / grid;
+}
+
+// The CTA whose range holds flattened block w: the largest c with
+// work_begin(c) <= w.
+__device__ __forceinline__ int work_owner(long long work, int grid, long long w) {
+  return (int)(((w + 1) * grid - 1) / work);
+}
+
+// One tile's part of a CTA's range: K blocks [kb0, kb1) of the tile; slot -1
+// when that is the whole tile (y written directly), else the CTA's partial
+// slot (0 for the first tile of its range, 1 for the last).
+struct Seg {
+  int mt, nt, kb0, kb1, slot;
 };
 
-__device__ __forceinline__ Unit decode(const Params& p, int u) {
-  Unit x;
-  x.tile = u / p.S;
-  x.s = u - x.tile * p.S;
-  x.mt = x.tile % p.mtiles;
-  x.nt = x.tile / p.mtiles;
-  x.kb0 = (int)((long long)p.kblocks * x.s / p.S);
-  x.kb1 = (int)((long long)p.kblocks * (x.s + 1) / p.S);
+__device__ __forceinline__ Seg segment(const Params& p, int tile, long long w0, long long w1, int first_tile) {
+  Seg x;
+  x.mt = tile % p.mtiles;
+  x.nt = tile / p.mtiles;
+  const long long base = (long long)tile * p.kblocks, end = base + p.kblocks;
+  x.kb0 = (int)((w0 > base ? w0 : base) - base);
+  x.kb1 = (int)((w1 < end ? w1 : end) - base);
+  x.slot = (x.kb0 == 0 && x.kb1 == p.kblocks) ? -1 : (tile == first_tile ? 0 : 1);
   return x;
 }
 
@@ -106,17 +129,18 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
+  // This CTA's K blocks (non-empty: the grid is at most the block count).
+  const long long w0 = work_begin(p.work, p.grid, blockIdx.x), w1 = work_begin(p.work, p.grid, blockIdx.x + 1);
+  const int t_first = (int)(w0 / p.kblocks), t_last = (int)((w1 - 1) / p.kblocks);
   if (warp == 0 && lane == 0) {
     tma_prefetch(&tm_w);
     tma_prefetch(&tm_x);
     // The weights are not written while the layers of a pass run: while an
     // earlier kernel on the stream finishes, bring this CTA's first ring's
     // worth of weight boxes into L2 (x, an earlier layer's output, waits).
-    if ((int)blockIdx.x < p.units) {
-      const Unit x = decode(p, blockIdx.x);
-      const int kend = x.kb1 < x.kb0 + p.stages ? x.kb1 : x.kb0 + p.stages;
-      for (int kb = x.kb0; kb < kend; ++kb) tma_prefetch_l2_2d(&tm_w, kb * 64, x.mt * 128);
-    }
+    const Seg x = segment(p, t_first, w0, w1, t_first);
+    const int kend = x.kb1 < x.kb0 + p.stages ? x.kb1 : x.kb0 + p.stages;
+    for (int kb = x.kb0; kb < kend; ++kb) tma_prefetch_l2_2d(&tm_w, kb * 64, x.mt * 128);
   }
   tc_fence_before();
   __syncthreads();
@@ -131,8 +155,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     if (lane == 0) {
       int g = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < p.units && alive; u += gridDim.x) {
-        const Unit x = decode(p, u);
+      for (int t = t_first; t <= t_last && alive; ++t) {
+        const Seg x = segment(p, t, w0, w1, t_first);
         for (int kb = x.kb0; kb < x.kb1; ++kb, ++g) {
           const int s = g % p.stages;
           if (g >= p.stages &&
@@ -154,8 +178,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     const uint32_t idesc = idesc_bf16_f32(128, p.TN, false, false);
     int g = 0, tc = 0;
     bool alive = true;
-    for (int u = blockIdx.x; u < p.units && alive; u += gridDim.x, ++tc) {
-      const Unit x = decode(p, u);
+    for (int t = t_first; t <= t_last && alive; ++t, ++tc) {
+      const Seg x = segment(p, t, w0, w1, t_first);
       const int ab = tc & 1;
       if (tc >= 2 && !(alive = warp_wait(&bars->acc_empty[ab], ((tc >> 1) - 1) & 1, &s_abort))) break;
       tc_fence_after();
@@ -187,15 +211,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     const int m = threadIdx.x - 128;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
     int tc = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++tc) {
-      const Unit x = decode(p, u);
+    for (int t = t_first; t <= t_last; ++t, ++tc) {
+      const Seg x = segment(p, t, w0, w1, t_first);
       const int ab = tc & 1;
       if (!warp_wait(&bars->acc_full[ab], (tc >> 1) & 1, &s_abort)) break;
       tc_fence_after();
       const int n = x.mt * 128 + m;      // output feature of this thread
       const int t0 = x.nt * p.TN;        // first token of the tile
-      const bool direct = p.S == 1;
-      float* pbase = direct ? nullptr : p.part + ((size_t)x.tile * p.S + x.s) * p.TN * 128 + m;
+      const bool direct = x.slot < 0;
+      float* pbase = direct ? nullptr : p.part + ((size_t)blockIdx.x * 2 + x.slot) * p.TN * 128 + m;
       for (int c = 0; c < p.TN; c += 32) {
         float v[32];
         tmem_ld32(lane_addr + ab * 256 + c, v);
@@ -228,42 +252,77 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Split K: y[t][n] = bf16(sum over s of the partials), s in order.  One thread
-// per 4 consecutive output features of a token: the partials are feature
-// fastest, so each split is one 16-byte load (all S issued before the first
-// add) and the result one 8-byte store (element stores at a ragged feature
-// tail or when Nout is not a multiple of 4).
+// Shared tiles: y = bf16(sum of the tile's partials, in CTA order).  Block x
+// looks at the boundary between CTAs x and x + 1; when it falls inside a tile
+// and no earlier boundary falls inside the same tile, the block adds that
+// tile's partials for kReduceCols of its token columns (blockIdx.y): lane l
+// takes output features 4l..4l+3 (one 16-byte load per contributing CTA and
+// column), warp w columns 2w and 2w + 1.  The loads of four CTAs for both
+// columns are issued before their adds (the sum stays in CTA order), and each
+// result is one 8-byte store (element stores at a ragged feature tail or when
+// Nout is not a multiple of 4).
 __global__ void __launch_bounds__(256)
 linear_reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, int T, int Nout, int TN,
-                     int mtiles, int S) {
+                     int mtiles, int kblocks, long long work, int grid) {
+  using namespace lin;
   pdl_wait();
   pdl_trigger();
-  const int nq = (Nout + 3) >> 2;  // feature quads per token
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (size_t)T * nq) return;
-  const int t = (int)(i / nq), n = (int)(i - (size_t)t * nq) * 4;
-  const int tile = (t / TN) * mtiles + n / 128, col = t % TN, row = n % 128;
-  const float4* src = reinterpret_cast<const float4*>(part + (((size_t)tile * S) * TN + col) * 128 + row);
-  const size_t step = (size_t)TN * 128 / 4;  // one split, in float4
-  float4 v[lin::kMaxSplit];
+  const int c = blockIdx.x + 1;  // first CTA after the boundary
+  const long long wc = work_begin(work, grid, c);
+  if (wc % kblocks == 0) return;  // on a tile edge: no tile shared here
+  const int tile = (int)(wc / kblocks);
+  const long long base = (long long)tile * kblocks;
+  const long long wp = work_begin(work, grid, c - 1);
+  if (wp > base) return;  // the boundary before this one is inside the same tile and takes it
+  const int mt = tile % mtiles, nt = tile / mtiles;
+  const int row = (threadIdx.x & 31) * 4, n = mt * 128 + row;
+  if (n >= Nout) return;
+  const int c_hi = work_owner(work, grid, base + kblocks - 1);
+  const size_t slot_elems = (size_t)TN * 128;
+  // CTA c - 1 holds the tile's first part: in its slot 0 when the tile is the
+  // first of its range (it starts at the tile's first block), else slot 1; the
+  // later CTAs start inside the tile, so it is their first (slot 0).
+  const float* first = part + ((size_t)(c - 1) * 2 + (wp == base ? 0 : 1)) * slot_elems;
+  const int col0 = blockIdx.y * kReduceCols + (threadIdx.x >> 5) * 2;
+  bool ok[2];
+  size_t off[2];
+  float4 acc[2];
 #pragma unroll
-  for (int s = 0; s < lin::kMaxSplit; ++s)
-    if (s < S) v[s] = __ldcg(src + s * step);
-  float a0 = v[0].x, a1 = v[0].y, a2 = v[0].z, a3 = v[0].w;
+  for (int i = 0; i < 2; ++i) {
+    const int col = col0 + i;
+    ok[i] = col < TN && nt * TN + col < T;
+    off[i] = (size_t)col * 128 + row;
+    if (ok[i]) acc[i] = __ldcg(reinterpret_cast<const float4*>(first + off[i]));
+  }
+  for (int cc = c; cc <= c_hi; cc += 4) {
+    float4 v[2][4];
 #pragma unroll
-  for (int s = 1; s < lin::kMaxSplit; ++s)
-    if (s < S) {
-      a0 += v[s].x;
-      a1 += v[s].y;
-      a2 += v[s].z;
-      a3 += v[s].w;
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (cc + j <= c_hi && ok[i])
+          v[i][j] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(cc + j) * 2 * slot_elems + off[i]));
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (cc + j <= c_hi && ok[i]) {
+          acc[i].x += v[i][j].x;
+          acc[i].y += v[i][j].y;
+          acc[i].z += v[i][j].z;
+          acc[i].w += v[i][j].w;
+        }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (!ok[i]) continue;
+    uint16_t* out = y + (size_t)(nt * TN + col0 + i) * Nout + n;
+    if ((Nout & 3) == 0) {
+      *reinterpret_cast<uint2*>(out) = make_uint2(bf16x2_rn(acc[i].x, acc[i].y), bf16x2_rn(acc[i].z, acc[i].w));
+    } else {
+      const float a[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+      for (int j = 0; j < 4 && n + j < Nout; ++j) out[j] = (uint16_t)f32_to_bf16_bits(a[j]);
     }
-  uint16_t* out = y + (size_t)t * Nout + n;
-  if ((Nout & 3) == 0) {
-    *reinterpret_cast<uint2*>(out) = make_uint2(bf16x2_rn(a0, a1), bf16x2_rn(a2, a3));
-  } else {
-    const float a[4] = {a0, a1, a2, a3};
-    for (int j = 0; j < 4 && n + j < Nout; ++j) out[j] = (uint16_t)f32_to_bf16_bits(a[j]);
   }
 }
 
@@ -297,7 +356,9 @@ static bool linear_map(CUtensorMap* m, const void* base, int cols, long long row
 
 // Launch geometry shared by the workspace query and the call.
 struct LinearPlan {
-  int TN, mtiles, ntiles, S, kblocks, units, grid, stages;
+  int TN, mtiles, ntiles, kblocks, grid, stages;
+  long long work;
+  bool shared;  // some tile's K range spans two CTAs: partials and the reduce kernel
   uint32_t stage_bytes;
   size_t part_bytes;
 };
@@ -308,35 +369,18 @@ static LinearPlan linear_plan(int T, int K, int Nout) {
   L.ntiles = (T + L.TN - 1) / L.TN;
   L.mtiles = (Nout + 127) / 128;
   L.kblocks = (K + 63) / 64;
-  const int tiles = L.mtiles * L.ntiles;
-  const int sms = device_sm_count();
-  // Split K from a time model of this GPU (about 6.8 TB/s of HBM and 1.9
-  // PFLOP/s of dense bf16, shared by the SMs): a tile costs the larger of its
-  // MMA time and its weight-stream time on one SM; S splits run tiles * S
-  // units in ceil(tiles * S / SMs) rounds and add the fp32 partials (written
-  // and read back once) to the HBM traffic.
-  const double sm_flops = 1.9e15 / sms, sm_bw = 6.8e12 / sms, hbm = 6.8e12;
-  const double t_tile = fmax(2.0 * 128 * L.TN * (double)K / sm_flops, 128.0 * 2 * (double)K / sm_bw);
-  L.S = 1;
-  int max_s = L.kblocks / 4 > 1 ? L.kblocks / 4 : 1;  // at least 4 K blocks per unit
-  if (max_s > lin::kMaxSplit) max_s = lin::kMaxSplit;
-  double best = 1e30;
-  for (int S = 1; S <= max_s; ++S) {
-    const double rounds = (double)((tiles * S + sms - 1) / sms);
-    const double cost = rounds * t_tile / S + (S > 1 ? (double)S * tiles * 128.0 * L.TN * 8.0 / hbm : 0.0);
-    if (cost < best * (1.0 - 1e-9)) {
-      best = cost;
-      L.S = S;
-    }
-  }
-  L.units = tiles * L.S;
-  const int rounds = (L.units + sms - 1) / sms;
-  L.grid = (L.units + rounds - 1) / rounds;
+  L.work = (long long)L.mtiles * L.ntiles * L.kblocks;
+  // One CTA per SM, each with an equal share of the K blocks (at least
+  // kMinBlocksPerCta of them).
+  long long g = L.work / lin::kMinBlocksPerCta;
+  if (g > device_sm_count()) g = device_sm_count();
+  L.grid = g < 1 ? 1 : (int)g;
+  L.shared = false;
+  for (int c = 1; c < L.grid && !L.shared; ++c) L.shared = lin::work_begin(L.work, L.grid, c) % L.kblocks != 0;
   L.stage_bytes = lin::kATile + (uint32_t)L.TN * 128;
   L.stages = (int)(lin::kRingBytes / L.stage_bytes);
   if (L.stages > lin::kMaxStages) L.stages = lin::kMaxStages;
-  L.part_bytes = L.S > 1 ? (size_t)tiles * L.S * 128 * L.TN * sizeof(float) : 0;
-
+  L.part_bytes = L.shared ? (size_t)L.grid * 2 * L.TN * 128 * sizeof(float) : 0;
   return L;
 }
 
@@ -372,24 +416,23 @@ static medusa_status linear_call(const void* x, const void* w, void* y, int T, i
   p.TN = L.TN;
   p.mtiles = L.mtiles;
   p.ntiles = L.ntiles;
-  p.S = L.S;
   p.kblocks = L.kblocks;
-  p.units = L.units;
+  p.grid = L.grid;
+  p.work = L.work;
   p.stages = L.stages;
   p.stage_bytes = L.stage_bytes;
   p.y = static_cast<uint16_t*>(y);
-  p.part = L.S > 1 ? static_cast<float*>(ws) : nullptr;
+  p.part = L.shared ? static_cast<float*>(ws) : nullptr;
   p.d_status = d_status;
   p.withhold_first = withhold_first;
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lin::kSmemBytes) !=
       cudaSuccess)
     return MEDUSA_ERR_CUDA;
   launch_pdl(linear_tc_kernel, dim3(L.grid), dim3(lin::kThreads), lin::kSmemBytes, s, mw, mx, p);
-  if (L.S > 1) {
-    const size_t quads = (size_t)T * ((Nout + 3) / 4);
-    launch_pdl(linear_reduce_kernel, dim3((unsigned)((quads + 255) / 256)), dim3(256), 0, s,
-               static_cast<const float*>(ws), p.y, T, Nout, L.TN, L.mtiles, L.S);
-  }
+  if (L.shared)
+    launch_pdl(linear_reduce_kernel, dim3((unsigned)(L.grid - 1), (unsigned)((L.TN + lin::kReduceCols - 1) / lin::kReduceCols)),
+               dim3(256), 0, s,
+               static_cast<const float*>(ws), p.y, T, Nout, L.TN, L.mtiles, L.kblocks, L.work, L.grid);
   return launch_status();
 }
 

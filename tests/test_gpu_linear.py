@@ -2,8 +2,9 @@
 float64 oracle.  bf16 output: every element within 2^-8 |ref| + 1e-3 rms(ref)
 (one bf16 rounding of an fp32 sum), and the whole tensor within the bf16
 tolerance.  Shapes cover one and several token tiles, ragged token, feature
-and K tails, split-K (deterministic: repeated calls are bit-identical) and the
-7B verify pass's layer shapes at 64 tree tokens."""
+and K tails, tiles whose K range is shared by two to 43 CTAs (partials added
+in a fixed order: repeated calls are bit-identical) and the 7B verify pass's
+layer shapes at 64 tree tokens."""
 import numpy as np
 import pytest
 
@@ -58,7 +59,7 @@ def test_linear_parity(mg, T, K, N):
 
 def test_linear_split_k_is_deterministic_and_reuses_its_workspace(mg):
     T, K, N = 64, 4096, 4096
-    assert mg.lib().medusa_linear_workspace_size(T, K, N) > 0  # this shape splits K
+    assert mg.lib().medusa_linear_workspace_size(T, K, N) > 0  # tiles shared by several CTAs
     x, w = _inputs(T, K, N, 3)
     dx, dw = to_dev(x), to_dev(w)
     ws = torch.empty(mg.lib().medusa_linear_workspace_size(T, K, N), dtype=torch.uint8, device="cuda")
@@ -85,6 +86,8 @@ MORE_SHAPES = [
     (256, 1024, 1408),  # full 256-token tile, 11 weight tiles
     (1000, 512, 768),   # four token tiles, ragged last one
     (96, 4096, 2176),   # 96-token tile, split K
+    (16, 11008, 128),   # one tile whose 172 K blocks are shared by 43 CTAs
+    (512, 4096, 4160),  # two token tiles, ragged feature tile, ranges crossing token tiles
 ]
 
 
