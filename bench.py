@@ -173,6 +173,10 @@ def run_ours(args, c):
                                                   stream),
                 "accept": lambda: vs.accept(d["logits"], stream),
                 "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}.get(args.profile)
+        if args.profile == "linear":  # the 8-layer verify pass (807 MB of weights) at 64 tree tokens
+            lp = LinearPass(mg, c, dev)
+            lp.tokens(64)
+            call = lambda: lp.run(stream)  # noqa: E731
         if args.profile == "head_loss":  # one sequence of 512 tokens: 262 MB of logits (above L2)
             lc, z, y = loss_inputs(dev, "f32", B=1, S=512)
             gz = torch.empty_like(z)
@@ -395,36 +399,53 @@ def time_linear(mg, c, stream, dev, reps):
     return out
 
 
-def time_linear_chain(mg, c, stream, dev, reps=10):
+class LinearPass:
     """The verify pass's linear layers of one Vicuna-7B-shape transformer layer
     (qkv 4096 -> 12288, o 4096 -> 4096, gate_up 4096 -> 22016, down 11008 -> 4096),
-    two layers' worth of distinct weights (807 MB, above L2) run back to back as
-    a verify pass runs them, over the tree tokens of B = 1, 4 and 16 rows at 64
-    nodes.  Weights are synthetic N(0, 0.02) bf16 drawn on the device."""
+    two layers' worth of distinct weights (807 MB, above L2), run back to back as
+    a verify pass runs them.  Weights are synthetic N(0, 0.02) bf16 drawn on the
+    device from a seeded generator."""
+
+    def __init__(self, mg, c, dev):
+        import torch
+        self.mg, self.dev = mg, dev
+        H, I = c["H"], 11008
+        self.shapes = [(H, 3 * H), (H, H), (H, 2 * I), (I, H)]
+        self.g = torch.Generator(device=dev).manual_seed(1)
+        self.layers = [(K, N, (torch.randn((N, K), generator=self.g, device=dev) * 0.02).to(torch.bfloat16))
+                       for _ in range(2) for K, N in self.shapes]
+        self.weight_bytes = sum(2 * K * N for K, N, _ in self.layers)
+
+    def tokens(self, T):
+        """Inputs, outputs and workspace for T tree tokens."""
+        import torch
+        self.T = T
+        self.xs = {K: torch.randn((T, K), generator=self.g, device=self.dev).to(torch.bfloat16)
+                   for K in {K for K, _ in self.shapes}}
+        self.ys = {N: torch.empty((T, N), dtype=torch.bfloat16, device=self.dev) for _, N in self.shapes}
+        self.ws = torch.empty(max(1, max(self.mg.lib().medusa_linear_workspace_size(T, K, N) for K, N in self.shapes)),
+                              dtype=torch.uint8, device=self.dev)
+
+    def run(self, s):
+        for K, N, w in self.layers:
+            self.mg.medusa_linear(self.xs[K], w, self.ys[N], ws=self.ws, stream=s)
+
+
+def time_linear_chain(mg, c, stream, dev, reps=10):
+    """LinearPass over the tree tokens of B = 1, 4 and 16 rows at 64 nodes."""
     import torch
     hbm, tflops, _ = _peaks()
-    H, I = c["H"], 11008
-    shapes = [(H, 3 * H), (H, H), (H, 2 * I), (I, H)]
-    g = torch.Generator(device=dev).manual_seed(1)
-    layers = [(K, N, (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16))
-              for _ in range(2) for K, N in shapes]
-    wbytes = sum(2 * K * N for K, N, _ in layers)
+    lp = LinearPass(mg, c, dev)
+    wbytes = lp.weight_bytes
     out = {"layers": "qkv, o, gate_up, down x 2 (Vicuna-7B shapes)", "weight_bytes": wbytes}
     for B in (1, 4, 16):
         T = B * 64
-        xs = {K: torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16) for K in (H, I)}
-        ys = {N: torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _, N in shapes}
-        ws = torch.empty(max(1, max(mg.lib().medusa_linear_workspace_size(T, K, N) for K, N in shapes)),
-                         dtype=torch.uint8, device=dev)
-
-        def chain(s):
-            for K, N, w in layers:
-                mg.medusa_linear(xs[K], w, ys[N], ws=ws, stream=s)
+        lp.tokens(T)
         for _ in range(3):
-            chain(stream)
+            lp.run(stream)
         # the 8 calls (up to 16 launches) as one CUDA graph, replayed back to
         # back: device time only, the host's per-call cost is not on the path
-        gr = _capture(chain)
+        gr = _capture(lp.run)
         for _ in range(3):
             gr.replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -434,12 +455,12 @@ def time_linear_chain(mg, c, stream, dev, reps=10):
         b.record(stream)
         torch.cuda.synchronize()
         us = a.elapsed_time(b) / reps * 1e3
-        flops = sum(2.0 * T * K * N for K, N, _ in layers)
-        out[f"T{T}"] = {"us_per_layer": round(us / len(layers), 2), "weight_gbs": round(wbytes / us / 1e3, 1),
+        flops = sum(2.0 * T * K * N for K, N, _ in lp.layers)
+        out[f"T{T}"] = {"us_per_layer": round(us / len(lp.layers), 2), "weight_gbs": round(wbytes / us / 1e3, 1),
                         "hbm_frac": round(wbytes / us / 1e3 / hbm, 4), "tflops": round(flops / us / 1e6, 1),
                         "tensor_frac": round(flops / us / 1e6 / tflops, 4)}
-        del gr, xs, ys, ws
-    del layers
+        del gr
+    del lp
     return out
 
 
@@ -674,7 +695,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
-    ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope", "head_loss"], default=None,
+    ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope", "linear", "head_loss"], default=None,
                     help="run only this call `steps` times after warm-up (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
