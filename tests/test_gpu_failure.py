@@ -23,7 +23,7 @@ def mg():
 
 
 def test_linear_bounded_wait_reports_timeout_and_context_survives(mg):
-    T, K, N = 64, 256, 256  # one K split, fewer K blocks than ring stages
+    T, K, N = 64, 256, 256  # two CTAs with one whole tile each, fewer K blocks than ring stages
     rng = np.random.default_rng(3)
     x = wl.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
     w = wl.to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))

@@ -40,12 +40,12 @@ def _check(y, ref):
 SHAPES = [
     (1, 64, 100),       # one token, one ragged feature tile
     (17, 8, 1),         # K shorter than one 64-column block, a single output feature
-    (64, 4096, 4096),   # 7B o_proj at 64 tree tokens (split K)
+    (64, 4096, 4096),   # 7B o_proj at 64 tree tokens (tiles shared by five or six CTAs)
     (300, 256, 384),    # two token tiles, ragged token tail
     (256, 4096, 1000),  # full 256-token tile, ragged feature tail
     (1024, 512, 1024),  # many tiles, several units per CTA
     (40, 520, 136),     # K not a multiple of 64
-    (32, 2048, 1002),   # split K with a feature count that is not a multiple of 4
+    (32, 2048, 1002),   # shared tiles with a feature count that is not a multiple of 4
 ]
 
 
@@ -57,7 +57,7 @@ def test_linear_parity(mg, T, K, N):
     _check(to_host(y), oracle.linear(x, w))
 
 
-def test_linear_split_k_is_deterministic_and_reuses_its_workspace(mg):
+def test_linear_shared_tiles_are_deterministic_and_reuse_the_workspace(mg):
     T, K, N = 64, 4096, 4096
     assert mg.lib().medusa_linear_workspace_size(T, K, N) > 0  # tiles shared by several CTAs
     x, w = _inputs(T, K, N, 3)
@@ -81,11 +81,11 @@ def test_linear_vicuna7b_layers_at_64_tree_tokens(mg, K, N):
 
 
 MORE_SHAPES = [
-    (16, 2048, 1152),   # 16-token tile, 9 weight tiles, split K
-    (64, 2048, 640),    # 5 weight tiles, split K
+    (16, 2048, 1152),   # 16-token tile, 9 weight tiles, shared tiles
+    (64, 2048, 640),    # 5 weight tiles, each shared by eight CTAs
     (256, 1024, 1408),  # full 256-token tile, 11 weight tiles
     (1000, 512, 768),   # four token tiles, ragged last one
-    (96, 4096, 2176),   # 96-token tile, split K
+    (96, 4096, 2176),   # 96-token tile, shared tiles
     (16, 11008, 128),   # one tile whose 172 K blocks are shared by 43 CTAs
     (512, 4096, 4160),  # two token tiles, ragged feature tile, ranges crossing token tiles
 ]
