@@ -697,10 +697,16 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope", "linear", "head_loss"], default=None,
                     help="run only this call `steps` times after warm-up (profiler captures)")
+    ap.add_argument("--profile-nodes", type=int, default=None,
+                    help="with --profile: a greedy sparse tree of this many nodes instead of 64")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile_nodes is not None and not args.profile:
+        ap.error("--profile-nodes applies to --profile runs only")
     c = wl.config("7b")
+    if args.profile_nodes is not None:
+        c = wl.config("7b", tree=(c["tree"][0], c["tree"][1], args.profile_nodes))
     if args.impl == "reference":
         run_reference(args, c)
     else:

@@ -131,14 +131,14 @@ ATTN_CASES = [
     dict(name="tiny", dtype="bf16", nl=1, B=1, Hq=2, Hkv=1, d=64, L=40, tree=("paths", []), Ls=[40]),
     dict(name="tiny", dtype="bf16", nl=1, B=2, Hq=2, Hkv=2, d=128, L=130, tree=("dense", (4, 4, 4, 4), 256),
          Ls=[130, 1]),
-    # tensor-core path: two kv heads per tile, odd kv-head count, prefix an exact tile multiple
+    # tensor-core path: odd kv-head count, prefix an exact tile multiple
     dict(name="tiny", dtype="bf16", nl=1, B=2, Hq=6, Hkv=3, d=128, L=100, tree=("dense", (2, 2, 2), 15),
          Ls=[100, 64]),
     # GQA group of 2 with 64 nodes: 128 rows per tile, empty prefix
     dict(name="tiny", dtype="bf16", nl=2, B=1, Hq=4, Hkv=2, d=128, L=20, tree=("greedy", 10, 64), Ls=[0]),
     # a single node (plain decode) on one kv head
     dict(name="tiny", dtype="bf16", nl=1, B=1, Hq=1, Hkv=1, d=128, L=5, tree=("paths", []), Ls=[5]),
-    # GQA group of 8 packed two heads per tile
+    # GQA group of 8 (16 query rows per kv head)
     dict(name="tiny", dtype="bf16", nl=1, B=3, Hq=16, Hkv=2, d=128, L=130, tree=("dense", (2, 2), 7),
          Ls=[130, 1, 63]),
     # more work items than SMs: every CTA runs several items through the pipeline
@@ -202,7 +202,7 @@ def test_tree_attention_ignores_rows_past_prefix(mg):
 
 
 @pytest.mark.parametrize("Hq,Hkv,tree", [(4, 4, ("dense", (2, 2, 2), 15)), (8, 2, ("greedy", 10, 64))],
-                         ids=["two-heads-per-tile", "128-row-tiles"])
+                         ids=["few-rows-per-head", "128-row-tiles"])
 def test_tree_attention_scores_growing_over_tiles(mg, Hq, Hkv, tree):
     """Key blocks scaled up along the prefix (x4, then x8; tree keys x2), so a
     row's running maximum grows by far more than 2^8 after its first tiles and
@@ -220,6 +220,38 @@ def test_tree_attention_scores_growing_over_tiles(mg, Hq, Hkv, tree):
     kc = wl.to_bf16_bits(kf)
     kt = wl.to_bf16_bits(wl.bf16_bits_to_f32(kt) * 2.0)
     _, _, mask = otopo.tree_build(t, np.zeros(2, np.int32), np.zeros((2, max(1, t.max_depth), 10), np.int32), pl)
+    ref = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    st = _status(mg)
+    out = mg.medusa_tree_attention(to_dev(q), to_dev(kc), to_dev(vc), to_dev(kt), to_dev(vt),
+                                   to_dev(mask.view(np.int32)), to_dev(pl), d_status=st)
+    torch.cuda.synchronize()
+    assert rel_err(bf16_to_f64(to_host(out)), ref) <= TOL["bf16"]
+    assert mg.medusa_status_check(st) == 0
+
+
+@pytest.mark.parametrize("Hq,growing", [(2, False), (4, True)], ids=["G1", "G2-growing-scores"])
+def test_tree_attention_two_kv_heads_per_tile(mg, Hq, growing):
+    """The tensor-core path packs two kv heads into one 128-row tile (block-
+    diagonal P) when a head has at most 64 query rows: here one packed item per
+    SM (layers = SM count, two kv heads), so the persistent grid runs exactly
+    one round.  With growing=True the key blocks grow along the prefix so the
+    output is rescaled mid-row."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = 64 // (Hq // 2)
+    c = wl.config("tiny", dtype="bf16", nl=sms, B=1, Hq=Hq, Hkv=2, d=128, L=200,
+                  tree=("greedy", 10, N))
+    t = _topo(c)
+    assert t.n_nodes * (Hq // 2) <= 64
+    pl = np.array([200], np.int32)
+    q = wl.queries(c, t.n_nodes)
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, t.n_nodes)
+    if growing:
+        kf = wl.bf16_bits_to_f32(kc)
+        kf[:, :, 64:128] *= 4.0
+        kf[:, :, 128:200] *= 8.0
+        kc = wl.to_bf16_bits(kf)
+    _, _, mask = otopo.tree_build(t, np.zeros(1, np.int32), np.zeros((1, max(1, t.max_depth), 10), np.int32), pl)
     ref = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
     st = _status(mg)
     out = mg.medusa_tree_attention(to_dev(q), to_dev(kc), to_dev(vc), to_dev(kt), to_dev(vt),
