@@ -173,3 +173,33 @@ def test_host_validation_rejects_before_launch():
     assert L.medusa_head_loss_workspace_size(4, 4, 2048) == 48 + 4 * 4 * 2048 * 4
     assert L.medusa_head_loss_workspace_size(33, 1, 1) == 0
     assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"
+
+
+def _linear_scratch(T, K, N, sms=152):
+    """The linear layer's scratch from its stated division: tiles of 128 features
+    by TN tokens, the K blocks of all tiles end to end divided over
+    G = min(SMs, blocks / 4) CTAs; two fp32 partial slots of 128 x TN per CTA
+    when some CTA boundary falls inside a tile, else none."""
+    TN = (T + 15) // 16 * 16 if T <= 256 else 256
+    kb = (K + 63) // 64
+    work = ((N + 127) // 128) * ((T + TN - 1) // TN) * kb
+    G = max(1, min(sms, work // 4))
+    shared = any((work * c // G) % kb for c in range(1, G))
+    return G * 2 * TN * 128 * 4 if shared else 0
+
+
+def test_linear_workspace_follows_the_even_k_division():
+    """Host planning without a GPU (152 SMs assumed): known sizes, and the rule
+    over random shapes."""
+    L = binding.lib()
+    assert L.medusa_linear_workspace_size(64, 4096, 4096) == 152 * 2 * 64 * 128 * 4   # o_proj, 64 tokens
+    assert L.medusa_linear_workspace_size(256, 4096, 4096) == 152 * 2 * 256 * 128 * 4
+    assert L.medusa_linear_workspace_size(1024, 4096, 4096) == 152 * 2 * 256 * 128 * 4
+    assert L.medusa_linear_workspace_size(64, 256, 256) == 0     # two CTAs, one whole tile each
+    assert L.medusa_linear_workspace_size(300, 256, 384) == 0    # 24 blocks on 6 CTAs: tile edges
+    assert L.medusa_linear_workspace_size(17, 8, 1) == 0         # one block, one CTA
+    assert L.medusa_linear_workspace_size(0, 64, 64) == 0 and L.medusa_linear_workspace_size(8, 64, 0) == 0
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        T, K, N = int(rng.integers(1, 3000)), 8 * int(rng.integers(1, 1500)), int(rng.integers(1, 6000))
+        assert L.medusa_linear_workspace_size(T, K, N) == _linear_scratch(T, K, N), (T, K, N)
