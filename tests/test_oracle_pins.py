@@ -300,6 +300,33 @@ def test_each_node_equals_attention_on_prefix_plus_ancestor_path(G):
                 np.testing.assert_allclose(out[0, b, i, hq], ref, rtol=1e-12, atol=1e-12)
 
 
+def test_nodes_of_a_256_node_tree_equal_attention_on_their_ancestor_paths():
+    """The same brute force on the 256-node dense tree (4 x 4 x 4 x 4, capped),
+    whose ancestor mask spans eight 32-bit words per row: nodes from every word,
+    including the last, against the key list built from parent pointers alone
+    (so a wrong word or bit index in the mask would show)."""
+    c = wl.config("tiny", nl=1, B=1, Hq=4, Hkv=2, d=8, L=5)
+    t = topo_mod.dense([4, 4, 4, 4], max_nodes=256)
+    assert t.n_nodes == 256
+    pl = np.array([5], np.int32)
+    q, kc, vc, kt, vt, mask = _attn_inputs(c, t, pl)
+    assert mask.shape[-1] == 8
+    out = oracle.tree_attention(q, kc, vc, kt, vt, mask, pl)
+    for i in list(range(0, 256, 7)) + [31, 32, 63, 64, 224, 254, 255]:
+        anc = []
+        a = i
+        while a >= 0:
+            anc.append(a)
+            a = t.parent[a]
+        anc = anc[::-1]
+        for hq in range(c["Hq"]):
+            g = hq // 2
+            keys = np.concatenate([kc[0, 0, :5, g], kt[0, 0, anc, g]], 0)
+            vals = np.concatenate([vc[0, 0, :5, g], vt[0, 0, anc, g]], 0)
+            ref = _sdpa(q[0, 0, i, hq][None], keys, vals, 1 / math.sqrt(c["d"]))[0]
+            np.testing.assert_allclose(out[0, 0, i, hq], ref, rtol=1e-12, atol=1e-12)
+
+
 def test_single_node_is_plain_decode_attention_and_gqa_grouping():
     """N = 1 is decode attention; q head h reads kv head h // G (torch enable_gqa)."""
     c = wl.config("tiny", nl=1, B=1, Hq=8, Hkv=2, d=16, L=33)
