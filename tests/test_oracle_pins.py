@@ -510,6 +510,37 @@ def test_kv_compact_chain_full_accept_is_identity_and_other_rows_untouched():
         np.testing.assert_array_equal(kc2[:, b, L + N:], kc[:, b, L + N:])
 
 
+def test_kv_compact_branching_path_gathers_its_nodes():
+    """On a branching tree the path's node ids differ from its depths: row L + i
+    of every layer's K and V cache receives tree row path[i] (i < accept_len),
+    and no other cache row changes."""
+    c = wl.config("tiny", nl=3, B=2, Hkv=2, d=8, L=12, dtype="bf16")
+    t = topo_mod.dense([2, 2, 2])
+    N = t.n_nodes
+    kc, vc = wl.kv_cache(c)
+    kt, vt = wl.tree_kv(c, N)
+    pl = np.array([12, 5], np.int32)
+    path = np.full((2, t.max_depth + 1), -1, np.int32)
+    for b, leaf in enumerate((N - 1, N - 4)):
+        nodes, a = [], leaf
+        while a >= 0:
+            nodes.append(a)
+            a = t.parent[a]
+        path[b, :len(nodes)] = nodes[::-1]
+    acc = np.array([t.max_depth + 1, 2], np.int32)
+    assert any(path[b, i] != i for b in range(2) for i in range(acc[b]))
+    kc2, vc2, new_len, ovf = oracle.kv_compact(kc, vc, kt, vt, path, acc, pl)
+    assert not ovf.any() and list(new_len) == [12 + acc[0], 5 + acc[1]]
+    for b in range(2):
+        L, A = pl[b], acc[b]
+        for i in range(A):
+            np.testing.assert_array_equal(kc2[:, b, L + i], kt[:, b, path[b, i]])
+            np.testing.assert_array_equal(vc2[:, b, L + i], vt[:, b, path[b, i]])
+        for x2, x in ((kc2, kc), (vc2, vc)):
+            np.testing.assert_array_equal(x2[:, b, :L], x[:, b, :L])
+            np.testing.assert_array_equal(x2[:, b, L + A:], x[:, b, L + A:])
+
+
 def test_kv_compact_overflow_writes_nothing():
     c = wl.config("tiny", nl=1, B=2, Hkv=1, d=4, L=4)
     kc, vc = wl.kv_cache(c)  # Lmax = L + slack
