@@ -442,6 +442,28 @@ def test_temperature_zero_is_argmax_match():
         assert r["next_tok"][b] == am[b, r["path_nodes"][b, r["accept_len"][b] - 1]]
 
 
+def test_planted_first_children_are_accepted_to_full_depth():
+    """At temperature 0, a tree whose every internal node puts its first child's
+    token at the top of its logits (max + 4) accepts the whole first-child chain:
+    accept_len = D + 1, path = root and the first child at each depth (canonical
+    order: 0, 1, 4, 13 on the 3 x 3 x 3 tree), next token = argmax at the leaf."""
+    c = wl.config("tiny", V=64, B=3)
+    t = topo_mod.dense([3, 3, 3])
+    N = t.n_nodes
+    tokens = wl.random_tokens(c, N)
+    logits = wl.base_logits(c, N).astype(np.float32)
+    for n in range(N):
+        kids = [m for m in range(N) if t.parent[m] == n]
+        if kids:
+            for b in range(3):
+                logits[b, n, tokens[b, kids[0]]] = logits[b, n].max() + 4.0
+    r = oracle.typical_accept(logits, tokens, t.parent, T=0.0, eps=0.09, delta=0.3)
+    assert list(r["accept_len"]) == [4, 4, 4]
+    for b in range(3):
+        assert list(r["path_nodes"][b]) == [0, 1, 4, 13]
+        assert r["next_tok"][b] == int(np.argmax(logits[b, 13]))
+
+
 def test_root_always_accepted_prefix_and_and_longest_path():
     """First token accepted unconditionally; no accepted node under a rejected one;
     accept_len = depth of the deepest accepted node + 1; path is root..best."""
