@@ -590,99 +590,71 @@ def run_e2e(args, c, vs, inp, d, dev, stream):
                        "kernels of step i (two device input sets)"}
 
 
-def oracle_sample(c, inp, topo_o, small=False, whole=False):
-    """Times the float64 oracle on one verify step.
-
-    whole: every call of the step in full (heads, packing, attention over all
-    layers, acceptance, compaction over all layers): nothing extrapolated.
-    Otherwise a bounded sample scaled to the step by multiply-add counts:
-    heads in full, tree attention on layer 0 (x nl), compaction on layer 0
-    (x nl); small: head 0 with the first V/8 vocabulary rows and attention on
-    layer 0 and the first 4 kv heads (x nl*Hkv/4)."""
-    import oracle
-    from oracle import topology as otopo
-    K, H, V = c["K"], c["H"], c["V"]
+def oracle_sample(c, inp, topo_o):
+    """Times the float64 oracle on one whole verify step, every call in full
+    (heads, packing, attention over all layers, acceptance, compaction over all
+    layers): nothing extrapolated.  Returns (seconds, description)."""
+    from oracle import step as ostep
     t0 = time.perf_counter()
-    if small:
-        vs = max(c["topk"], V // 8)
-        heads = oracle.heads(inp["h"], inp["w1"][:1], inp["w2"][:1, :vs], c["topk"])
-        heads_scale = K * (H * H + V * H) / (H * H + vs * H)
-        idx = np.repeat(heads["idx"], K, axis=1)
-    else:
-        heads = oracle.heads(inp["h"], inp["w1"], inp["w2"], c["topk"])
-        heads_scale = 1.0
-        idx = heads["idx"]
-    t1 = time.perf_counter()
-    tokens, pos, mask = otopo.tree_build(topo_o, inp["root_tok"], idx, inp["prefix_len"])
-    t2 = time.perf_counter()
-    G = c["Hq"] // c["Hkv"]
-    nkv = 4 if small else c["Hkv"]
-    nl_s = c["nl"] if whole else 1
-    q = np.ascontiguousarray(inp["q"][:nl_s, :, :, :nkv * G])
-    kc, vc = np.ascontiguousarray(inp["kc"][:nl_s, :, :, :nkv]), np.ascontiguousarray(inp["vc"][:nl_s, :, :, :nkv])
-    kt, vt = np.ascontiguousarray(inp["kt"][:nl_s, :, :, :nkv]), np.ascontiguousarray(inp["vt"][:nl_s, :, :, :nkv])
-    t2b = time.perf_counter()
-    oracle.tree_attention(q, kc, vc, kt, vt, mask, inp["prefix_len"])
-    t3 = time.perf_counter()
-    attn_scale = c["nl"] * c["Hkv"] / (nkv * nl_s)
-    acc = oracle.typical_accept(inp["logits"], tokens, topo_o.parent, c["T"], c["eps"], c["delta"],
-                                Dmax=topo_o.max_depth)
-    t4 = time.perf_counter()
-    oracle.kv_compact(inp["kc"][:nl_s], inp["vc"][:nl_s], inp["kt"][:nl_s], inp["vt"][:nl_s], acc["path_nodes"],
-                      acc["accept_len"], inp["prefix_len"])
-    t5 = time.perf_counter()
-    step_s = (t1 - t0) * heads_scale + (t2 - t1) + (t3 - t2b) * attn_scale + (t4 - t3) + (t5 - t4) * c["nl"] / nl_s
-    work = (t1 - t0) + (t2 - t1) + (t3 - t2b) + (t4 - t3) + (t5 - t4)
-    if whole:
-        sample = (f"one whole verify step, nothing extrapolated: heads, tree packing, tree attention over all "
-                  f"{c['nl']} layers, typical acceptance, KV compaction over all layers; {work:.2f} s of CPU work, "
-                  f"single thread")
-        return step_s, sample, work
-    if small:
-        what = (f"head 0 on the first {V // 8} of {V} vocabulary rows (x{heads_scale:.1f} by MACs), "
-                f"tree attention on layer 0 x {nkv} of {c['Hkv']} kv heads (x{attn_scale:g})")
-    else:
-        what = f"heads in full, tree attention on layer 0 of {c['nl']} (x{attn_scale:g})"
-    sample = (f"{what}; tree packing and typical acceptance in full; KV compaction on layer 0 (x{c['nl']}); "
-              f"{work:.2f} s of CPU work per sample, single thread")
-    return step_s, sample, work
+    ostep.run_step(c, topo_o, inp, inp["logits"])
+    work = time.perf_counter() - t0
+    sample = (f"one whole verify step, nothing extrapolated: heads, tree packing, tree attention over all "
+              f"{c['nl']} layers, typical acceptance, KV compaction over all layers; {work:.2f} s of CPU work, "
+              f"single thread")
+    return work, sample
 
 
 def cpu_baseline(c, inp, topo):
     from oracle import topology as otopo
     topo_o = otopo.greedy(otopo.synthetic_accuracy(c["K"], c["tree"][1]), c["tree"][2])
-    step_s, sample, _ = oracle_sample(c, inp, topo_o, whole=True)
+    step_s, sample = oracle_sample(c, inp, topo_o)
     return {"value": round(1.0 / step_s, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
             "host_cpus": os.cpu_count()}
 
 
 def run_reference(args, c):
-    """The oracle as it stands, timed on the host cores (single thread)."""
+    """The oracle as it stands, timed on the host cores.
+
+    Every step is one whole verify step of the workload (heads, tree packing,
+    tree attention over all layers, typical acceptance, KV compaction over all
+    layers), nothing sampled or extrapolated.  The oracle itself is
+    single-threaded; independent steps run side by side on a pool of host
+    threads (the C oracle releases the interpreter lock while it computes), one
+    step per thread at a time.  value = steps / wall time of the timed steps."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import concurrent.futures as cf
+    from oracle import step as ostep
     from oracle import topology as otopo
     import oracle
     oracle.build()
+    oracle.oracle.lib()
     topo_o = otopo.greedy(otopo.synthetic_accuracy(c["K"], c["tree"][1]), c["tree"][2])
-    # Only layer 0 of the per-layer tensors is generated: the sample times one
-    # layer of attention and scales it (the oracle's cost does not depend on
-    # the values, so the logits are left unplanted here).
-    inp = make_inputs(c, topo_o.n_nodes, layers=[0])
-    for _ in range(args.warmup):
-        oracle_sample(c, inp, topo_o, small=True)
-    times, sample = [], ""
-    for _ in range(args.steps):
-        s, sample, _ = oracle_sample(c, inp, topo_o, small=True)
-        times.append(s)
-    ms = 1e3 * sum(times) / len(times)
-    value = 1e3 / ms
+    inp = make_inputs(c, topo_o.n_nodes)
+    inp["logits"] = wl.plant(c, inp["logits"], ostep.tree_tokens(c, topo_o, inp), topo_o.parent)
+    threads = max(1, min(os.cpu_count() or 1, 16, args.steps))
+
+    def one(_):
+        ostep.run_step(c, topo_o, inp, inp["logits"])
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(one, range(args.warmup)))
+        t0 = time.perf_counter()
+        list(ex.map(one, range(args.steps)))
+        wall = time.perf_counter() - t0
+    ms = 1e3 * wall / args.steps
+    value = args.steps / wall
+    sample = (f"{args.steps} whole verify steps of the workload (heads, tree packing, tree attention over all "
+              f"{c['nl']} layers, typical acceptance, KV compaction over all layers; nothing sampled or "
+              f"extrapolated), each a single-thread float64 oracle step, {threads} steps at a time on "
+              f"{threads} host threads; {wall:.1f} s wall")
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
                       "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
                       "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                       "data": "synthetic (seeded, model shapes)", "config": config_json(c, topo_o.n_nodes),
-                      "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                      "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
                                        "sample": sample, "host_cpus": os.cpu_count()},
                       "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                               "d2h_bytes_per_step": 0}}))

@@ -247,9 +247,11 @@ medusa_status medusa_typical_accept(const float* logits, const int32_t* tokens,
  *  - Limit: medusa_typical_accept_workspace_size(B, N, V) must not exceed
  *    MEDUSA_ACCEPT_NOALLOC_MAX_BYTES (1 MiB; e.g. B * N <= 4096 at V = 32000),
  *    else MEDUSA_ERR_UNSUPPORTED before any launch.
- *  - The first call on a device looks up the array's device address (a
- *    one-time runtime query, no allocation); make that first call before any
- *    stream capture on that device.  MEDUSA_ERR_CUDA if the lookup fails.
+ *  - Every call looks up the array's device address in the current context
+ *    (a runtime query; MEDUSA_ERR_CUDA if it fails).  The first call in a
+ *    context may load the library's device code, and that load is what
+ *    allocates the array: make the first call at start-up, before any stream
+ *    capture on that device (or load modules eagerly, CUDA_MODULE_LOADING=EAGER).
  *  - Every call on a device uses the same array and leaves its contents
  *    behind; each call writes every entry it reads first, so nothing needs
  *    clearing.  Calls whose kernels overlap on the GPU (different streams
@@ -315,15 +317,6 @@ medusa_status medusa_tree_rope(void* q, void* k, const int32_t* pos, int n_layer
 size_t medusa_linear_workspace_size(int T, int K, int Nout);
 medusa_status medusa_linear(const void* x, const void* w, void* y, int T, int K, int Nout, medusa_dtype dt,
                             void* ws, size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
-
-/* medusa_linear_test_stall: failure-detection test hook.  Runs medusa_linear
- * (bf16) with the first stage's loads withheld, so the kernel's bounded
- * barrier waits (1 s) expire: the kernel stops every role, drains its copies
- * and MMAs, frees its tensor memory and sets MEDUSA_DEV_TIMEOUT in d_status;
- * y is not meaningful.  The call leaves the context usable (no fault, no
- * trap).  Same arguments and validation as medusa_linear. */
-medusa_status medusa_linear_test_stall(const void* x, const void* w, void* y, int T, int K, int Nout, void* ws,
-                                       size_t ws_bytes, int32_t* d_status, medusa_stream_t stream);
 
 /* ------------------------------------------------- (h) online tree calibration
  * The sparse tree of the paper review ("方法细节") is built from per-head top-i

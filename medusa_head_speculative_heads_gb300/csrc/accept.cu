@@ -20,8 +20,6 @@
 // token.
 #include <limits.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "host_util.h"
 
@@ -171,7 +169,8 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
                    int32_t* __restrict__ accept_len, int32_t* __restrict__ path_nodes,
                    int32_t* __restrict__ next_tok, float* __restrict__ p_tok, float* __restrict__ thr_out,
                    int32_t* d_status) {
-  __shared__ int acc[MEDUSA_MAX_NODES], pass[MEDUSA_MAX_NODES], amax[MEDUSA_MAX_NODES], par[MEDUSA_MAX_NODES];
+  __shared__ int acc[MEDUSA_MAX_NODES], pass[MEDUSA_MAX_NODES], amax[MEDUSA_MAX_NODES], par[MEDUSA_MAX_NODES],
+      dep[MEDUSA_MAX_NODES];
   __shared__ float zmax[MEDUSA_MAX_NODES], ssum[MEDUSA_MAX_NODES], thr[MEDUSA_MAX_NODES];
   __shared__ int s_key[kSelectThreads / 32];
   __shared__ int s_bad;
@@ -222,9 +221,18 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   if (c < N) {
     dc = dc_ld;
     pc = pc_ld;
-    if (c > 0 && (pc < 0 || pc >= c || dc < 1 || dc > max_depth)) s_bad = 1;
     acc[c] = c == 0 ? 1 : 0;
     par[c] = pc;
+    dep[c] = dc;
+  }
+  __syncthreads();
+  // The level loop and the path walk below index shared memory with par[] and
+  // stop on depths: the root must be (parent -1, depth 0) and every other node
+  // must sit one level below an earlier node.
+  if (c < N) {
+    const bool bad = c == 0 ? (pc != -1 || dc != 0)
+                            : (pc < 0 || pc >= c || dc < 1 || dc > max_depth || dep[pc] != dc - 1);
+    if (bad) s_bad = 1;
   }
   __syncthreads();
   if (s_bad) {
@@ -358,21 +366,20 @@ namespace medusa {
 constexpr size_t kNoallocScratchBytes = MEDUSA_ACCEPT_NOALLOC_MAX_BYTES;
 static __device__ __align__(256) float4 g_accept_scratch[kNoallocScratchBytes / sizeof(float4)];
 
-// Device address of g_accept_scratch on each device (host code only sees a
-// host-side stand-in for the symbol; it must not be passed to a kernel).
-static std::mutex g_scratch_mu;
-static float4* g_scratch_ptr[64] = {nullptr};
-
+// Device address of g_accept_scratch in the current context.  Host code sees
+// only a host-side stand-in for the symbol, which must never reach a kernel.
+// The address is looked up on every call (a runtime query that allocates
+// nothing once this library's device code is loaded in the context), so a
+// context created after cudaDeviceReset gets its own array's address rather
+// than a stale one.  The first lookup in a context may load that device code,
+// which is when the array itself is allocated.
 static medusa_status accept_scratch(float4** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MEDUSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) return MEDUSA_ERR_CUDA;
-    g_scratch_ptr[dev] = static_cast<float4*>(p);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<float4*>(p);
   return MEDUSA_OK;
 }
 

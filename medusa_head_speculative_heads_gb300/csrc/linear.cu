@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "medusa_test_hooks.h"
 #include "host_util.h"
 #include "sm100.cuh"
 

@@ -129,6 +129,20 @@ def test_host_validation_rejects_before_launch():
     st.n_nodes = 7
     assert L.medusa_typical_accept(fake, fake, ctypes.byref(st), 1, 100, ctypes.c_float(0.5), ctypes.c_float(0.1),
                                    ctypes.c_float(0.3), fake, fake, fake, None, None, fake, 1 << 20, None, None) == 1
+    # the allocation-free acceptance call: a size whose statistics exceed its
+    # static array (256 rows x 256 nodes at V = 32000: 8 MiB > 1 MiB) is
+    # rejected with UNSUPPORTED before any launch; invalid arguments as above
+    assert L.medusa_typical_accept_workspace_size(256, 256, 32000) > (1 << 20)
+    st3 = binding.medusa_dev_topology()
+    st3.n_nodes, st3.max_depth = 256, 4
+    st3.parent = st3.depth = 4096
+    F32 = ctypes.c_float
+    assert L.medusa_typical_accept_noalloc(fake, fake, ctypes.byref(st3), 256, 32000, F32(0.7), F32(0.09),
+                                           F32(0.3), fake, fake, fake, None, None, None, None) == 2
+    assert L.medusa_typical_accept_noalloc(fake, fake, ctypes.byref(st), 1, 100, F32(0.5), F32(0.1), F32(0.3),
+                                           fake, fake, fake, None, None, None, None) == 1
+    assert L.medusa_typical_accept_noalloc(fake, fake, ctypes.byref(st3), 1, 100, F32(-1.0), F32(0.1),
+                                           F32(0.3), fake, fake, fake, None, None, None, None) == 1
     # tree_rope: odd or oversized head_dim, missing pos, q and k overlapping, bad base
     F = ctypes.c_float
     assert L.medusa_tree_rope(fake, P(base * 64), fake, 1, 1, 7, 4, 2, 63, F(1e4), 1, None) == 1

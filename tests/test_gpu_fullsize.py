@@ -9,7 +9,7 @@ import pytest
 import oracle
 from oracle import topology as otopo
 import workloads as wl
-from tests.helpers import TOL, bf16_to_f64, check_topk, rel_err, to_dev, to_host
+from tests.helpers import TOL, bf16_to_f64, check_accept, check_topk, rel_err, to_dev, to_host
 from tests.step import lib_topology
 
 torch = pytest.importorskip("torch")
@@ -37,16 +37,17 @@ def test_vicuna7b_shape_step_sampled_parity():
            d["logits"])
     torch.cuda.synchronize()
     assert vs.check() == 0
-    # heads
+    # heads: logits within tolerance, top-k exact up to flagged near-ties
     assert rel_err(to_host(z), heads["z"]) <= TOL["bf16"]
     checked, flagged = check_topk(to_host(vs.topk_idx), to_host(vs.topk_logit), heads["z"],
                                   lambda zz: 1e-4 * float(np.sqrt(np.mean(zz * zz))), TOL["bf16"])
-    assert flagged <= 1
-    gpu_idx = to_host(vs.topk_idx)
+    assert checked + flagged == c["K"] * c["topk"] and flagged <= 1
+    # tree packing of the GPU's own top-k (bit-exact); identical to the
+    # oracle's tokens whenever no top-k rank was flagged
+    g_tokens, g_pos, g_mask = otopo.tree_build(t, inp["root_tok"], to_host(vs.topk_idx), inp["prefix_len"])
+    np.testing.assert_array_equal(to_host(vs.tokens), g_tokens)
     if flagged == 0:
-        np.testing.assert_array_equal(gpu_idx, heads["idx"])
-        # tree packing (bit-exact, from the same top-k)
-        np.testing.assert_array_equal(to_host(vs.tokens), tokens)
+        np.testing.assert_array_equal(g_tokens, tokens)
     np.testing.assert_array_equal(to_host(vs.pos), pos)
     np.testing.assert_array_equal(to_host(vs.mask).view(np.uint32), mask)
     # tree attention on the first and last layers
@@ -56,13 +57,12 @@ def test_vicuna7b_shape_step_sampled_parity():
                                     inp["prefix_len"])
         got = bf16_to_f64(to_host(vs.attn_out[l:l + 1]))
         assert rel_err(got, ref) <= TOL["bf16"], l
-    # typical acceptance on the GPU's own tokens (identical to the oracle's when no near-tie was flagged)
+    # typical acceptance on the GPU's own tokens: exact, or one of the results
+    # the flagged near-threshold tests allow (no row skipped)
     acc = oracle.typical_accept(logits, to_host(vs.tokens), t.parent, c["T"], c["eps"], c["delta"], Dmax=t.max_depth)
-    near = np.abs(acc["p_tok"][0, 1:] - acc["thr"][0, 1:]) < 1e-6
-    if not near.any():
-        assert int(vs.accept_len[0]) == acc["accept_len"][0]
-        np.testing.assert_array_equal(to_host(vs.path_nodes), acc["path_nodes"])
-        assert int(vs.next_tok[0]) == acc["next_tok"][0]
+    compared, _, _ = check_accept(to_host(vs.accept_len), to_host(vs.path_nodes), to_host(vs.next_tok), logits, acc,
+                                  t.parent, c["T"], t.max_depth)
+    assert compared == 1
     # compaction: the cache rows after the prefix hold the accepted path's tree rows
     path = to_host(vs.path_nodes)[0]
     A = int(vs.accept_len[0])

@@ -11,7 +11,7 @@ import pytest
 import oracle
 from oracle import topology as otopo
 import workloads as wl
-from tests.helpers import TOL, bf16_to_f64, check_topk, rel_err, to_dev, to_host
+from tests.helpers import ACCEPT_BAND, TOL, bf16_to_f64, check_accept, check_topk, rel_err, to_dev, to_host
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -43,7 +43,16 @@ def _tau(dtype):
     dict(name="tiny", dtype="f32", B=5, H=264, V=2049, K=4, topk=32),
     dict(name="tiny", dtype="bf16", B=8, H=1024, V=4099, K=2, topk=1),
     dict(name="tiny", dtype="bf16", B=11, H=256, V=700, K=2, topk=4),
-])
+    # the tensor-core path at every padded batch it instantiates (16, 32, 48, 64
+    # columns per half): bf16, 4 <= B <= 64, H a multiple of 64; V not a
+    # multiple of the 128-row weight tile
+    dict(name="tiny", dtype="bf16", B=4, H=1024, V=8000, K=2, topk=10),
+    dict(name="tiny", dtype="bf16", B=17, H=1024, V=8000, K=2, topk=10),
+    dict(name="tiny", dtype="bf16", B=32, H=1024, V=8000, K=2, topk=10),
+    dict(name="tiny", dtype="bf16", B=33, H=1024, V=8000, K=2, topk=10),
+    dict(name="tiny", dtype="bf16", B=48, H=768, V=6001, K=3, topk=10),
+    dict(name="tiny", dtype="bf16", B=64, H=1024, V=8000, K=2, topk=10),
+], ids=lambda c: f"{c.get('dtype', 'f32')}-B{c.get('B', 1)}-H{c.get('H', 256)}-V{c.get('V', 1024)}")
 def test_heads_parity(mg, case):
     c = wl.config(**case)
     h = wl.hidden(c)
@@ -286,21 +295,16 @@ def _accept_case(mg, c, t, tokens, logits, T, eps, delta):
     torch.cuda.synchronize()
     assert mg.medusa_status_check(st) == 0
     al, pn, nt, pt, th = (to_host(x) for x in (al, pn, nt, pt, th))
-    flagged_rows = 0
-    for b in range(tokens.shape[0]):
-        near = np.abs(ref["p_tok"][b, 1:] - ref["thr"][b, 1:]) < 1e-6 if T > 0 else np.zeros(t.n_nodes - 1, bool)
-        if near.any():
-            # within 1e-6 of the threshold: flagged, not counted; the result must still be a valid path
-            agree = al[b] == ref["accept_len"][b] and np.array_equal(pn[b], ref["path_nodes"][b])
-            flagged_rows += 0 if agree else 1
-            assert 1 <= al[b] <= t.max_depth + 1
-            continue
-        assert al[b] == ref["accept_len"][b]
-        np.testing.assert_array_equal(pn[b], ref["path_nodes"][b])
-        assert nt[b] == ref["next_tok"][b]
-    assert np.max(np.abs(pt - ref["p_tok"])) <= 1e-5
-    assert rel_err(th[:, 1:], ref["thr"][:, 1:]) <= 1e-4
-    return ref, flagged_rows
+    # fp32 outputs: the probability of every node's token and its parent's threshold
+    assert rel_err(pt[:, 1:], ref["p_tok"][:, 1:]) <= TOL["f32"]
+    assert rel_err(th[:, 1:], ref["thr"][:, 1:]) <= TOL["f32"]
+    # the GPU's error of p - threshold stays inside the flag band, so every
+    # decision outside the band is the oracle's
+    err = np.max(np.abs((pt[:, 1:] - th[:, 1:]) - (ref["p_tok"][:, 1:] - ref["thr"][:, 1:])))
+    assert err < ACCEPT_BAND, err
+    compared, flagged, differs = check_accept(al, pn, nt, logits, ref, t.parent, T, t.max_depth)
+    assert compared == tokens.shape[0]
+    return ref, flagged
 
 
 @pytest.mark.parametrize("T,eps,delta,prob", [(0.0, 0.09, 0.3, 0.6), (0.7, 0.09, 0.3, 0.6), (1.0, 0.25, 0.5, 0.5),
