@@ -344,6 +344,33 @@ def test_typical_accept_bad_token_reports(mg):
     assert int(al[0]) in (1, 2)
 
 
+@pytest.mark.parametrize("fault", ["root_depth", "root_parent", "skipped_level", "same_level"])
+def test_typical_accept_bad_topology_reports(mg, fault):
+    """A caller-built device topology whose root or depths are inconsistent is
+    reported (BAD_TOPOLOGY) before any node is tested: the row keeps the root
+    alone and the next token is the root row's argmax."""
+    from medusa_head_speculative_heads_gb300 import binding
+    parent = [-1, 0, 0, 1, 1, 2, 2]
+    depth = [0, 1, 1, 2, 2, 2, 2]
+    {"root_depth": lambda: depth.__setitem__(0, 1), "root_parent": lambda: parent.__setitem__(0, 0),
+     "skipped_level": lambda: depth.__setitem__(3, 3), "same_level": lambda: depth.__setitem__(4, 1)}[fault]()
+    rank = [-1, 0, 1, 0, 1, 0, 1]
+    buf = torch.tensor(parent + depth + rank, dtype=torch.int32, device="cuda")
+    st = binding.medusa_dev_topology()
+    st.n_nodes, st.max_depth, st.n_leaves, st.max_rank = 7, 3, 4, 2
+    st.parent, st.depth, st.rank = buf.data_ptr(), buf.data_ptr() + 28, buf.data_ptr() + 56
+    dt = binding.DevTopology(st, buf)
+    c = wl.config("tiny", V=100, B=2)
+    logits = wl.base_logits(c, 7)
+    tokens = wl.random_tokens(c, 7)
+    sts = _status(mg)
+    al, pn, nt, _, _ = mg.medusa_typical_accept(to_dev(logits), to_dev(tokens), dt, 0.7, 0.09, 0.3, d_status=sts)
+    assert mg.medusa_status_check(sts) == 4  # BAD_TOPOLOGY
+    np.testing.assert_array_equal(to_host(al), [1, 1])
+    np.testing.assert_array_equal(to_host(pn), [[0, -1, -1, -1]] * 2)
+    np.testing.assert_array_equal(to_host(nt), np.argmax(logits[:, 0], axis=1))
+
+
 # ----------------------------------------------------------------------------- kv compaction
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
