@@ -140,10 +140,15 @@ def run_ours(args, c):
 
     topo = mg.Topology.greedy(np.array(wl.synthetic_accuracy(c["K"], c["tree"][1])), c["tree"][2])
     N = topo.n_nodes
-    inp = make_inputs(c, N)
     tdev = lambda a: _to_dev(a, dev)  # noqa: E731
-    d = {k: tdev(inp[k]) for k in ("h", "w1", "w2", "root_tok", "prefix_len", "q", "kc", "vc", "kt", "vt",
-                                   "logits")}
+    if args.profile:
+        # profiler runs: the same distributions drawn on the device (any batch fits)
+        inp = None
+        d = device_step_inputs(c, N, dev)
+    else:
+        inp = make_inputs(c, N)
+        d = {k: tdev(inp[k]) for k in ("h", "w1", "w2", "root_tok", "prefix_len", "q", "kc", "vc", "kt", "vt",
+                                       "logits")}
     vs = VerifyStep(B=c["B"], H=c["H"], V=c["V"], K=c["K"], topk=c["topk"], nl=c["nl"], Hq=c["Hq"], Hkv=c["Hkv"],
                     d=c["d"], Lmax=c["Lmax"], dtype=torch.bfloat16, topology=topo, temperature=c["T"],
                     eps=c["eps"], delta=c["delta"], device=dev)
@@ -152,9 +157,12 @@ def run_ours(args, c):
     vs.heads(d["h"], d["w1"], d["w2"])
     vs.tree(d["root_tok"], d["prefix_len"])
     torch.cuda.synchronize()
-    tokens = vs.tokens.cpu().numpy()
-    inp["logits"] = wl.plant(c, inp["logits"], tokens, topo.parent)
-    d["logits"] = tdev(inp["logits"])
+    if inp is None:
+        plant_on_device(c, d["logits"], vs.tokens, np.asarray(topo.parent))
+    else:
+        tokens = vs.tokens.cpu().numpy()
+        inp["logits"] = wl.plant(c, inp["logits"], tokens, topo.parent)
+        d["logits"] = tdev(inp["logits"])
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -258,6 +266,9 @@ def run_ours(args, c):
     linear = time_linear(mg, c, stream, dev, min(K, 50))
     linear_chain = time_linear_chain(mg, c, stream, dev)
     head_loss = time_head_loss(mg, stream, dev, min(K, 20))
+    configs = None
+    if args.configs != "none":
+        configs = time_configs(mg, stream, dev, min(K, 20), None if args.configs == "all" else args.configs.split(","))
 
     ms_per_step = elapsed_ms / K
     value = job_steps_per_s(ms_per_step, world)
@@ -285,7 +296,7 @@ def run_ours(args, c):
                 "accepted_tok_per_s": round(value * c["B"] * accept_len, 2), "mean_accept_len": accept_len,
                 "per_call_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
                 "roofline": roof, "rooflines": rooflines, "calibration": calib, "linear": linear, "linear_verify_pass": linear_chain,
-                "head_loss": head_loss, "e2e": e2e,
+                "head_loss": head_loss, "configs": configs, "e2e": e2e,
                 "cpu_baseline": cpu,
                 "gpu_launches": K * vs.launches_per_step(), "clocks": clocks}
         print(json.dumps(line))
@@ -511,6 +522,171 @@ def time_head_loss(mg, stream, dev, reps):
     return out
 
 
+# The other workloads of the verify step, each timed as a whole step (the five
+# calls in one CUDA graph): Vicuna-13B shape (batch 4, prefix 2048), the 7B-shape
+# batch sweep (1 to 64 rows, prefix 1024, greedy acceptance) and the Vicuna-33B
+# shape (prefix 4096) with the 64-node sparse and the 256-node dense tree.
+CONFIG_RUNS = (("13b_b4", "13b", None, "tree"), ("sweep_b1", "sweep", 1, "tree"), ("sweep_b8", "sweep", 8, "tree"),
+               ("sweep_b16", "sweep", 16, "tree"), ("sweep_b32", "sweep", 32, "tree"),
+               ("sweep_b64", "sweep", 64, "tree"), ("33b_sparse64", "33b", None, "tree"),
+               ("33b_dense256", "33b", None, "tree2"))
+
+
+def lib_topology(mg, c, which="tree"):
+    spec = c[which]
+    if spec[0] == "dense":
+        return mg.Topology.dense(list(spec[1]), spec[2])
+    return mg.Topology.greedy(np.array(wl.synthetic_accuracy(c["K"], spec[1])), spec[2])
+
+
+def device_step_inputs(c, N, dev):
+    """The workload's per-step inputs drawn on the device from a generator seeded
+    with the configuration id (same distributions as the seeded host recipe:
+    h, q, K, V ~ N(0, 1), weights ~ N(0, 0.02) in bf16, base logits ~ N(0, 2)
+    in fp32, root tokens uniform); per-layer tensors are drawn layer by layer."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(1000 + c["cfg_id"])
+    B, H, V, K, nl = c["B"], c["H"], c["V"], c["K"], c["nl"]
+    bf = torch.bfloat16
+
+    def normal(shape, std, out=None):
+        x = torch.randn(shape, generator=g, device=dev)
+        if std != 1.0:
+            x.mul_(std)
+        return x.to(bf) if out is None else out.copy_(x)
+
+    d = {"h": normal((B, H), 1.0), "w1": torch.empty((K, H, H), dtype=bf, device=dev),
+         "w2": torch.empty((K, V, H), dtype=bf, device=dev)}
+    for k in range(K):
+        normal((H, H), 0.02, d["w1"][k])
+        normal((V, H), 0.02, d["w2"][k])
+    shapes = {"q": (B, N, c["Hq"], c["d"]), "kc": (B, c["Lmax"], c["Hkv"], c["d"]),
+              "vc": (B, c["Lmax"], c["Hkv"], c["d"]), "kt": (B, N, c["Hkv"], c["d"]), "vt": (B, N, c["Hkv"], c["d"])}
+    for name, shp in shapes.items():
+        d[name] = torch.empty((nl,) + shp, dtype=bf, device=dev)
+        for l in range(nl):
+            normal(shp, 1.0, d[name][l])
+    d["logits"] = torch.randn((B, N, V), generator=g, device=dev).mul_(2.0)
+    d["root_tok"] = torch.randint(0, V, (B,), generator=g, device=dev, dtype=torch.int32)
+    d["prefix_len"] = torch.full((B,), c["L"], dtype=torch.int32, device=dev)
+    return d
+
+
+def plant_on_device(c, logits, tokens, parent):
+    """The workload's planting (for every node with children, with probability
+    p its first child's token gets the row maximum + 4), on device tensors; the
+    per-node draws come from the same seeded generators as the host recipe."""
+    import torch
+    B, N, V = logits.shape
+    first = np.full(N, -1)
+    for n in range(N - 1, 0, -1):
+        first[parent[n]] = n
+    hit = np.zeros((B, N), bool)
+    for b in range(B):
+        u = wl.rng(c["cfg_id"], wl.T_PLANT, 0, b).random(N)
+        hit[b] = (first >= 0) & (u < c["plant"])
+    bi, ni = np.nonzero(hit)
+    if len(bi) == 0:
+        return
+    bi_t = torch.from_numpy(bi).to(logits.device)
+    ni_t = torch.from_numpy(ni).to(logits.device)
+    ch_t = torch.from_numpy(first[ni]).to(logits.device)
+    tok = tokens[bi_t, ch_t].long()
+    rowmax = logits[bi_t, ni_t].amax(dim=1)
+    logits[bi_t, ni_t, tok] = rowmax + 4.0
+
+
+def config_algorithmic(c, N, mask_words):
+    """Algorithmic bytes of heads and tree attention, and the attention's
+    matrix-product flops over the visible keys (prefix + ancestors)."""
+    ab = algorithmic_bytes(c, N)
+    anc = sum(bin(int(w)).count("1") for w in np.asarray(mask_words, np.uint32).ravel())  # visible tree keys
+    flops = 4.0 * c["nl"] * c["B"] * c["Hq"] * c["d"] * (N * c["L"] + anc)
+    return ab["heads"], ab["attention"], flops
+
+
+def time_configs(mg, stream, dev, steps, names=None):
+    """Each workload of CONFIG_RUNS as a whole step: steps/s from graph replays
+    (device events), mean accept length on planted logits, per-call times from
+    an eager pass with events between the calls, and the heads / attention
+    fractions of the measured peaks."""
+    import torch
+    from medusa_head_speculative_heads_gb300.step import VerifyStep
+    hbm, tflops, _ = _peaks()
+    out = {}
+    for key, name, B, which in CONFIG_RUNS:
+        if names and key not in names:
+            continue
+        c = wl.config(name, **({} if B is None else {"B": B}))
+        topo = lib_topology(mg, c, which)
+        N = topo.n_nodes
+        d = device_step_inputs(c, N, dev)
+        vs = VerifyStep(B=c["B"], H=c["H"], V=c["V"], K=c["K"], topk=c["topk"], nl=c["nl"], Hq=c["Hq"],
+                        Hkv=c["Hkv"], d=c["d"], Lmax=c["Lmax"], dtype=torch.bfloat16, topology=topo,
+                        temperature=c["T"], eps=c["eps"], delta=c["delta"], device=dev)
+        vs.heads(d["h"], d["w1"], d["w2"], stream)
+        vs.tree(d["root_tok"], d["prefix_len"], stream)
+        torch.cuda.synchronize()
+        plant_on_device(c, d["logits"], vs.tokens, np.asarray(topo.parent))
+        args = (d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"], d["vt"],
+                d["logits"])
+        graph = vs.capture(*args)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        if vs.check() != 0:
+            raise RuntimeError(f"device status set in {key}")
+        acc_len = vs.accept_len.float().mean().item()
+        reps = max(3, min(steps, 10))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+        for i in range(reps):
+            e = ev[i]
+            e[0].record(stream)
+            vs.heads(d["h"], d["w1"], d["w2"], stream)
+            e[1].record(stream)
+            vs.tree(d["root_tok"], d["prefix_len"], stream)
+            e[2].record(stream)
+            vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"], stream)
+            e[3].record(stream)
+            vs.accept(d["logits"], stream)
+            e[4].record(stream)
+            vs.compact(d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"], stream)
+            e[5].record(stream)
+        torch.cuda.synchronize()
+        calls = ["heads", "tree_build", "attention", "accept", "compact"]
+        us = {n: 1e3 * sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(reps)) / reps
+              for j, n in enumerate(calls)}
+        hb, atb, atf = config_algorithmic(c, N, vs.mask.cpu().numpy().view(np.uint32))
+        heads_flops = 2.0 * c["B"] * c["K"] * (c["H"] * c["H"] + c["V"] * c["H"])
+        out[key] = {
+            "workload": f"{name} B={c['B']} H={c['H']} {c['nl']}x{c['Hq']}/{c['Hkv']}x{c['d']} prefix {c['L']} "
+                        f"{N}-node {c[which][0]} tree T={c['T']}",
+            "steps_per_s": round(1e3 / ms, 2), "ms_per_step": round(ms, 4),
+            "accepted_tok_per_s": round(1e3 / ms * c["B"] * acc_len, 1), "mean_accept_len": round(acc_len, 3),
+            "per_call_us": {k: round(v, 2) for k, v in us.items()},
+            "heads": {"gbs": round(hb / us["heads"] / 1e3, 1), "hbm_frac": round(hb / us["heads"] / 1e3 / hbm, 4),
+                      "tflops": round(heads_flops / us["heads"] / 1e6, 1)},
+            "attention": {"gbs": round(atb / us["attention"] / 1e3, 1),
+                          "hbm_frac": round(atb / us["attention"] / 1e3 / hbm, 4),
+                          "tflops": round(atf / us["attention"] / 1e6, 1),
+                          "tensor_frac": round(atf / us["attention"] / 1e6 / tflops, 4)},
+            "step_gbs": round((hb + atb) / ms / 1e6, 1),
+        }
+        del graph, vs, d
+        torch.cuda.empty_cache()
+    out["inputs"] = ("drawn on the device from a seeded generator (the host recipe's distributions), logits planted "
+                     "with the recipe's per-node draws; every input larger than L2, no flush")
+    out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tflops}
+    return out
+
+
 def max_over_ranks(elapsed_ms: float, world: int, device) -> float:
     """The slowest rank's timed region (every rank gets it)."""
     if world <= 1:
@@ -669,16 +845,23 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope", "linear", "head_loss"], default=None,
                     help="run only this call `steps` times after warm-up (profiler captures)")
+    ap.add_argument("--configs", default="all",
+                    help="other workloads timed as whole steps after the headline one: all, none, or a comma list of "
+                         + ", ".join(k for k, *_ in CONFIG_RUNS))
     ap.add_argument("--profile-nodes", type=int, default=None,
                     help="with --profile: a greedy sparse tree of this many nodes instead of 64")
+    ap.add_argument("--profile-batch", type=int, default=None,
+                    help="with --profile: the 7B-shape batch-sweep workload at this batch instead of batch 1")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.profile_nodes is not None and not args.profile:
-        ap.error("--profile-nodes applies to --profile runs only")
+    if (args.profile_nodes is not None or args.profile_batch is not None) and not args.profile:
+        ap.error("--profile-nodes / --profile-batch apply to --profile runs only")
     c = wl.config("7b")
+    if args.profile_batch is not None:
+        c = wl.config("sweep", B=args.profile_batch)
     if args.profile_nodes is not None:
-        c = wl.config("7b", tree=(c["tree"][0], c["tree"][1], args.profile_nodes))
+        c = wl.config(c["name"], B=c["B"], tree=(c["tree"][0], c["tree"][1], args.profile_nodes))
     if args.impl == "reference":
         run_reference(args, c)
     else:

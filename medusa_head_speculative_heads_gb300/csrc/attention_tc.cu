@@ -16,15 +16,21 @@
 // SM sub-partitions' exp units) busy.  Otherwise a tile holds 128 rows of one
 // kv head and 128 keys.
 //
-// Roles (256 threads): warp 0 lane 0 issues TMA (Q once per item; K and V of
-// every key tile into a six-slot ring of 32 KB half-tiles, a K slot freed as
-// soon as its S = Q K^T is done, a V slot when its P V is done); warp 1
-// allocates TMEM and lane 0 issues S = Q K^T into one of two S buffers; warp 2
-// lane 0 issues O += P V with P read from tensor memory; warps 4-7 (one row
-// per thread) read S from TMEM, apply the prefix-length / ancestor mask, keep
-// the online softmax in the log2 domain (O is rescaled in TMEM only when the
-// row maximum grows by more than 2^8), write P (bf16 pairs) into one of two
-// TMEM P buffers and finally normalise O and store the output.  With P double
+// Roles (128 + 128 x SPLIT threads): warp 0 lane 0 issues TMA (Q once per
+// item; K and V of every key tile into a six-slot ring of 32 KB half-tiles, a
+// K slot freed as soon as its S = Q K^T is done, a V slot when its P V is
+// done); warp 1 allocates TMEM and lane 0 issues S = Q K^T into one of two S
+// buffers; warp 2 lane 0 issues O += P V with P read from tensor memory; the
+// softmax warps from warp 4 on read S from TMEM, apply the prefix-length /
+// ancestor mask, keep the online softmax in the log2 domain (O is rescaled in
+// TMEM only when the row maximum grows by more than 2^8), write P (bf16 pairs)
+// into one of two TMEM P buffers and finally normalise O and store the
+// output.  With SPLIT = 2 each tile row has two softmax threads (warps 4-7 and
+// 8-11 read the same TMEM lane quarters), each with half of the row's scores,
+// half of P and half of O's columns: per tile they exchange their partial row
+// maxima through shared memory (an mbarrier per lane quarter and tile parity,
+// waited on with the same bound as every other wait) so both scale P by the
+// same maximum, and they add their partial row sums once per item.  With P double
 // buffered, the probabilities of tile t+1 wait only for the P V of tile t-1
 // (and for that of tile t only when O has to be rescaled), and with the two
 // MMA streams issued by different warps a score product never waits behind a
@@ -38,20 +44,32 @@
 #include "host_util.h"
 #include "sm100.cuh"
 
+// Softmax threads per row of a two-head (packed) tile: 1 or 2.
+#ifndef MEDUSA_ATTN_PACKED_SPLIT
+#define MEDUSA_ATTN_PACKED_SPLIT 1
+#endif
+
 namespace medusa {
 using namespace sm100;
 
 namespace tc {
 
-constexpr int kThreads = 256;
-constexpr int kSlots = 6;                               // ring of K or V half-tiles
+// Threads of a CTA: warps 0-3 (TMA, two MMA issuers, one idle) and SPLIT
+// groups of four softmax warps.
+__host__ __device__ constexpr int threads_for(int split) { return 128 + 128 * split; }
+constexpr int kMaxSlots = 6;                            // ring of K or V half-tiles
 constexpr uint32_t kHalf = 16384;                       // 128 rows x 128 bytes
 constexpr uint32_t kBox = 8192;                         // 64 rows x 128 bytes
 constexpr uint32_t kOffQ = 0;                           // 2 d-halves
 constexpr uint32_t kOffRing = 2 * kHalf;                // slot = K or V of one tile (2 d-halves)
 constexpr uint32_t kSlotBytes = 2 * kHalf;
-constexpr uint32_t kOffBar = kOffRing + kSlots * kSlotBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+// Ring slots: six with one softmax thread per row; five with two, whose
+// exchange buffers take static shared memory a sixth slot would need.
+__host__ __device__ constexpr int slots_for(int split) { return split == 2 ? 5 : kMaxSlots; }
+__host__ __device__ constexpr uint32_t off_bar(int split) { return kOffRing + slots_for(split) * kSlotBytes; }
+__host__ __device__ constexpr uint32_t smem_bytes(int split) {
+  return off_bar(split) + 512 + 1024;  // barriers + alignment slack
+}
 constexpr uint32_t kTmemCols = 512;                     // S0, S1, O (128 each), P0, P1 (64 each)
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 384;                         // P buffer b at kColP + 64 b (bf16 pairs)
@@ -76,8 +94,10 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t full[kSlots], empty[kSlots];
+  uint64_t full[kMaxSlots], empty[kMaxSlots];
   uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_free, drain, drain_pv;
+  uint64_t mx[2][4];  // SPLIT = 2: partial row maxima of a tile exchanged (tile parity, lane quarter)
+  uint64_t lx[4];     // SPLIT = 2: partial row sums of an item exchanged (lane quarter)
 };
 
 // Load sequence of one item of T key tiles: for j = 0 .. T + kLag - 1, K(j)
@@ -85,10 +105,12 @@ struct Bars {
 // the PVs, which wait for their tile's softmax, so each V tile is loaded about
 // kLag tiles after its K and lands when its PV is due instead of holding a
 // ring slot.  Both MMA issuers walk this sequence; half-tile c of the whole
-// sequence (items back to back, 2T each) uses ring slot c % kSlots.
+// sequence (items back to back, 2T each) uses ring slot c % NS (NS slots).
 constexpr int kLag = 2;
-__device__ __forceinline__ int slot_of(int c) { return c % kSlots; }
-__device__ __forceinline__ uint32_t use_parity(int c) { return (uint32_t)(c / kSlots) & 1u; }
+template <int NS>
+__device__ __forceinline__ int slot_of(int c) { return c % NS; }
+template <int NS>
+__device__ __forceinline__ uint32_t use_parity(int c) { return (uint32_t)(c / NS) & 1u; }
 
 struct Item {
   int lb, b, h0, mt, L, T, n_pre;
@@ -140,17 +162,23 @@ __device__ __forceinline__ Item decode(const Params& p, int it) {
 
 }  // namespace tc
 
-template <bool PACKED>
-__global__ void __launch_bounds__(tc::kThreads, 1)
+template <bool PACKED, int SPLIT>
+__global__ void __launch_bounds__(tc::threads_for(SPLIT), 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                     const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
                     const __grid_constant__ CUtensorMap tm_vt, const tc::Params p) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  constexpr int kSlots = slots_for(SPLIT);
+  static_assert(sizeof(Bars) <= 512, "barrier area");
+  Bars* bars = reinterpret_cast<Bars*>(smem + off_bar(SPLIT));
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  // SPLIT = 2: the two halves' partial row maxima (tile parity, half, row) and sums
+  __shared__ float s_mx[SPLIT == 2 ? 2 : 1][SPLIT][SPLIT == 2 ? 128 : 1];
+  __shared__ float s_l[SPLIT][SPLIT == 2 ? 128 : 1];
+  constexpr int kSoft = 128 * SPLIT;  // softmax threads
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -163,11 +191,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 128);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->s_free[s], kSoft);
+      mbar_init(&bars->p_full[s], kSoft);
       mbar_init(&bars->pv_done[s], 1);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->mx[s][q], 32 * SPLIT);
     }
-    mbar_init(&bars->o_free, 128);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->lx[q], 32 * SPLIT);
+    mbar_init(&bars->o_free, kSoft);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->drain_pv, 1);
     fence_mbar_init();
@@ -231,9 +261,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (t < 0 || t >= x.T) continue;
             const bool tree = t >= x.n_pre;
             const int j0 = (tree ? t - x.n_pre : t) * p.KT;
-            const int sl = slot_of(c);
+            const int sl = slot_of<kSlots>(c);
             if (c >= kSlots &&
-                !(alive = mbar_wait_bounded(&bars->empty[sl], use_parity(c - kSlots), &s_abort, kWaitNs)))
+                !(alive = mbar_wait_bounded(&bars->empty[sl], use_parity<kSlots>(c - kSlots), &s_abort, kWaitNs)))
               break;
             const CUtensorMap* mp = kv ? (tree ? &tm_vt : &tm_vc) : (tree ? &tm_kt : &tm_kc);
             uint8_t* dst = smem + kOffRing + sl * kSlotBytes;
@@ -252,7 +282,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // phase issued on every load barrier, so no copy lands after exit.
         if (n > 0) mbar_wait_bounded(&bars->q_full, (n - 1) & 1, nullptr, kDrainNs);
         for (int c = issued - 1; c >= 0 && c >= issued - kSlots; --c)
-          mbar_wait_bounded(&bars->full[slot_of(c)], use_parity(c), nullptr, kDrainNs);
+          mbar_wait_bounded(&bars->full[slot_of<kSlots>(c)], use_parity<kSlots>(c), nullptr, kDrainNs);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -280,12 +310,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (j < x.T) {
           const int gj = g0 + j, ck = c++, sb = gj & 1;
           if (s_role) {
-            if (!(alive = warp_wait(&bars->full[slot_of(ck)], use_parity(ck), &s_abort))) break;
+            if (!(alive = warp_wait(&bars->full[slot_of<kSlots>(ck)], use_parity<kSlots>(ck), &s_abort))) break;
             if (gj >= 2 && !(alive = warp_wait(&bars->s_free[sb], ((gj >> 1) - 1) & 1, &s_abort))) break;
             tc_fence_after();
             if (lane == 0) {
               const uint32_t qa = smem_u32(smem + kOffQ);
-              const uint32_t ka = smem_u32(smem + kOffRing + slot_of(ck) * kSlotBytes);
+              const uint32_t ka = smem_u32(smem + kOffRing + slot_of<kSlots>(ck) * kSlotBytes);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -293,7 +323,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                          kIdescQK, kk > 0);
               }
               mma_commit(&bars->s_full[sb]);
-              mma_commit(&bars->empty[slot_of(ck)]);
+              mma_commit(&bars->empty[slot_of<kSlots>(ck)]);
               if (j == x.T - 1) mma_commit(&bars->q_empty);
             }
             __syncwarp();
@@ -304,8 +334,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!s_role) {
             if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
             if (!(alive = warp_wait(&bars->p_full[gt & 1], (gt >> 1) & 1, &s_abort))) break;
-            if (!(alive = warp_wait(&bars->full[slot_of(cv)], use_parity(cv), &s_abort))) break;
-            uint8_t* vb = smem + kOffRing + slot_of(cv) * kSlotBytes;
+            if (!(alive = warp_wait(&bars->full[slot_of<kSlots>(cv)], use_parity<kSlots>(cv), &s_abort))) break;
+            uint8_t* vb = smem + kOffRing + slot_of<kSlots>(cv) * kSlotBytes;
             // The last prefix tile may run past prefix_len: zero those V rows
             // (stale cache rows may hold anything, and 0 * NaN is NaN).
             const int j0 = t * p.KT;
@@ -330,7 +360,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                             (kk > 0 || t > 0) ? 1u : 0u);
               }
               mma_commit(&bars->pv_done[gt & 1]);
-              mma_commit(&bars->empty[slot_of(cv)]);
+              mma_commit(&bars->empty[slot_of<kSlots>(cv)]);
             }
             __syncwarp();
           }
@@ -347,20 +377,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int q4 = warp - 4, m = threadIdx.x - 128;
+    // Softmax warp sw: lane quarter q4 (rows 32 q4 .. 32 q4 + 31 of the tile)
+    // and half `half` of each row's scores, P columns and O columns.
+    const int sw = warp - 4, q4 = sw & 3, half = sw >> 2;
+    const int m = 32 * q4 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
-    const int slot = PACKED ? (m >> 6) : 0;          // warp-uniform
-    constexpr int ncol = PACKED ? 64 : 128;
-    const int col0 = PACKED ? 64 * slot : 0;
+    const int slot = PACKED ? (m >> 6) : 0;             // warp-uniform
+    constexpr int NC = (PACKED ? 64 : 128) / SPLIT;     // score columns per thread
+    constexpr int OC = 128 / SPLIT;                     // O / output columns per thread
+    const int koff = NC * half;                         // first key of this thread within the tile's keys
+    const int scol = (PACKED ? 64 * slot : 0) + koff;   // its first S column (and 2 x its first P column)
     // Packed tiles: each row's P columns outside its own head block stay zero.
-    if (PACKED) {
+    if (PACKED && half == 0) {
       uint32_t z[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0u;
       for (int b = 0; b < 2; ++b) tmem_st32u(lane_addr + kColP + 64 * b + 32 * (1 - slot), z);
       tmem_wait_st();
     }
-    int g = 0;
+    int g = 0, nf = 0;
     bool alive = true;
     // The epilogue of an item (O / l -> bf16 output row, after the item's last
     // PV) runs, for two-head tiles, inside the next item's first tile after
@@ -372,23 +407,32 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     float pend_l = 0.f;
     int pend_g = 0;
     auto finish = [&]() -> bool {
+      float l = pend_l;
+      if constexpr (SPLIT == 2) {
+        // the row sum is the two halves' partial sums (same maximum, same scale)
+        s_l[half][m] = pend_l;
+        mbar_arrive(&bars->lx[q4]);
+        if (!warp_wait(&bars->lx[q4], nf & 1, &s_abort)) return false;
+        l = s_l[0][m] + s_l[1][m];
+      }
+      ++nf;
       if (!warp_wait(&bars->pv_done[pend_g & 1], (pend_g >> 1) & 1, &s_abort)) return false;
       tc_fence_after();
-      const float inv = pend_l > 0.f ? 1.f / pend_l : 0.f;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       // O in chunks of EC columns (one TMEM wait per chunk; 128-row tiles use
       // narrower chunks, their softmax already holds most registers).
-      constexpr int EC = PACKED ? 64 : 32;
+      constexpr int EC = (PACKED ? 64 : 32) < OC ? (PACKED ? 64 : 32) : OC;
 #pragma unroll
-      for (int h2 = 0; h2 < 128 / EC; ++h2) {
+      for (int h2 = 0; h2 < OC / EC; ++h2) {
         float o[EC];
 #pragma unroll
-        for (int q = 0; q < EC / 32; ++q) tmem_ld32(lane_addr + kColO + EC * h2 + 32 * q, o + 32 * q);
+        for (int q = 0; q < EC / 32; ++q) tmem_ld32(lane_addr + kColO + OC * half + EC * h2 + 32 * q, o + 32 * q);
         tmem_wait_ld();
         if (pend_ok) {
           uint32_t w[EC / 2];
 #pragma unroll
           for (int e = 0; e < EC / 2; ++e) w[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
-          uint16_t* dst = pend_row + EC * h2;
+          uint16_t* dst = pend_row + OC * half + EC * h2;
           if (p.out32) {
 #pragma unroll
             for (int q = 0; q < EC / 16; ++q) st_global_v8(dst + 16 * q, w + 8 * q);
@@ -418,42 +462,43 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int sb = g & 1;
         if (!(alive = warp_wait(&bars->s_full[sb], (g >> 1) & 1, &s_abort))) break;
         tc_fence_after();
-        float s[ncol];
-        tmem_ld32(lane_addr + sb * 128 + col0, s);
-        tmem_ld32(lane_addr + sb * 128 + col0 + 32, s + 32);
-        if constexpr (!PACKED) {
-          tmem_ld32(lane_addr + sb * 128 + 64, s + 64);
-          tmem_ld32(lane_addr + sb * 128 + 96, s + 96);
-        }
+        float s[NC];
+#pragma unroll
+        for (int q = 0; q < NC / 32; ++q) tmem_ld32(lane_addr + sb * 128 + scol + 32 * q, s + 32 * q);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars->s_free[sb]);
 
         const bool tree = t >= x.n_pre;
-        const int j0 = (tree ? t - x.n_pre : t) * p.KT;
+        const int j0 = (tree ? t - x.n_pre : t) * p.KT + koff;  // key of s[0]
         const float sc = p.scale_log2;
         // Raw-score maximum over the visible keys (scale > 0 keeps the order).
         float mx = -INFINITY;
-        if (!tree && j0 + p.KT <= x.L && row_ok) {
-          // a prefix tile entirely inside the prefix: every key is visible
+        if (!tree && j0 + NC <= x.L && row_ok) {
+          // keys entirely inside the prefix: every one is visible
 #pragma unroll
-          for (int c = 0; c < ncol; ++c) mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < NC; ++c) mx = fmaxf(mx, s[c]);
         } else {
-          uint32_t mw[4] = {0u, 0u, 0u, 0u};
-          if (tree && row_ok) {
+          uint32_t mw[NC / 32];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const int word = (j0 >> 5) + w;
-              if (w * 32 < ncol && word < p.W) mw[w] = p.mask[(size_t)node * p.W + word];
-            }
+          for (int w = 0; w < NC / 32; ++w) {
+            const int word = (j0 >> 5) + w;
+            mw[w] = (tree && row_ok && word < p.W) ? p.mask[(size_t)node * p.W + word] : 0u;
           }
 #pragma unroll
-          for (int c = 0; c < ncol; ++c) {
+          for (int c = 0; c < NC; ++c) {
             const int j = j0 + c;
             const bool v = row_ok && (tree ? (j < p.N && ((mw[c >> 5] >> (c & 31)) & 1u)) : (j < x.L));
             s[c] = v ? s[c] : -INFINITY;
             mx = fmaxf(mx, s[c]);
           }
+        }
+        if constexpr (SPLIT == 2) {
+          // both halves of the row continue with the maximum over all its keys
+          s_mx[sb][half][m] = mx;
+          mbar_arrive(&bars->mx[sb][q4]);
+          if (!(alive = warp_wait(&bars->mx[sb][q4], (g >> 1) & 1, &s_abort))) break;
+          mx = fmaxf(s_mx[sb][0][m], s_mx[sb][1][m]);
         }
         const float m_new = fmaxf(m_used, mx * sc);  // log2 domain
         const bool need = m_new > m_used + 8.f;
@@ -462,10 +507,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // Probabilities first (overlaps the previous tile's PV), packed to bf16.
         // exp2(-inf) = 0 covers the masked keys.
         float rs = 0.f;
-        uint32_t pk[ncol / 2];
+        uint32_t pk[NC / 2];
         const float neg = -m_used;
 #pragma unroll
-        for (int c = 0; c < ncol; c += 2) {
+        for (int c = 0; c < NC; c += 2) {
           const float a = m_used == -INFINITY ? 0.f : fast_exp2(fmaf(s[c], sc, neg));
           const float b2 = m_used == -INFINITY ? 0.f : fast_exp2(fmaf(s[c + 1], sc, neg));
           rs += a + b2;
@@ -479,12 +524,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           tc_fence_after();
           float o[32];
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            tmem_ld32(lane_addr + kColO + 32 * c4, o);
+          for (int c4 = 0; c4 < OC / 32; ++c4) {
+            tmem_ld32(lane_addr + kColO + OC * half + 32 * c4, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= f;
-            tmem_st32(lane_addr + kColO + 32 * c4, o);
+            tmem_st32(lane_addr + kColO + OC * half + 32 * c4, o);
           }
         }
         // P buffer g & 1 is free once the PV of tile g - 2 has read it.
@@ -493,8 +538,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!(alive = warp_wait(&bars->pv_done[pb], ((g - 2) >> 1) & 1, &s_abort))) break;
           tc_fence_after();
         }
-        tmem_st32u(lane_addr + kColP + 64 * pb + (PACKED ? 32 * slot : 0), pk);
-        if constexpr (!PACKED) tmem_st32u(lane_addr + kColP + 64 * pb + 32, pk + 32);
+        const uint32_t pa = lane_addr + kColP + 64 * pb + (scol >> 1);
+        if constexpr (NC / 2 == 16) {
+          tmem_st16u(pa, pk);
+        } else {
+#pragma unroll
+          for (int q = 0; q < NC / 64; ++q) tmem_st32u(pa + 32 * q, pk + 32 * q);
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[pb]);
@@ -613,15 +663,20 @@ medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, c
     cuuint32_t box[4] = {64, 1, 64, 1};
     if (!make_map(&mkt, kt, 4, dims, str, box) || !make_map(&mvt, vt, 4, dims, str, box)) return MEDUSA_ERR_CUDA;
   }
-  auto kern = p.packed ? tree_attn_tc_kernel<true> : tree_attn_tc_kernel<false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes) != cudaSuccess)
+  // 128-row tiles (trees above 64 nodes, GQA groups) split every row over two
+  // softmax threads; two-head tiles keep one thread per row.
+  constexpr int kSplitPacked = MEDUSA_ATTN_PACKED_SPLIT;
+  auto kern = p.packed ? tree_attn_tc_kernel<true, kSplitPacked> : tree_attn_tc_kernel<false, 2>;
+  const int threads = tc::threads_for(p.packed ? kSplitPacked : 2);
+  const uint32_t smem = tc::smem_bytes(p.packed ? kSplitPacked : 2);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
   // Equal-cost items: as many rounds as the SM count forces, then spread the
   // items evenly over just enough CTAs (no ragged last round).
   const int sms = device_sm_count();
   const int rounds = (p.items + sms - 1) / sms;
   const int grid = (p.items + rounds - 1) / rounds;
-  launch_pdl(kern, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, s, mq, mkc, mvc, mkt, mvt, p);
+  launch_pdl(kern, dim3(grid), dim3(threads), smem, s, mq, mkc, mvc, mkt, mvt, p);
   return launch_status();
 }
 

@@ -2,6 +2,8 @@
 algorithmic bytes per call on the Vicuna-7B shape step, counted here tensor by
 tensor from the shapes (weights, cache, tree K/V, q and out, node logits), and
 the whole-job rate of N replicas."""
+import numpy as np
+
 import bench
 import workloads as wl
 
@@ -30,3 +32,20 @@ def test_whole_job_rate_counts_every_replica():
     assert bench.job_steps_per_s(0.5, 1) == 2000.0
     assert bench.job_steps_per_s(0.5, 4) == 8000.0
     assert bench.max_over_ranks(3.25, 1, "cpu") == 3.25
+
+
+def test_device_planting_follows_the_host_recipe():
+    """bench.plant_on_device (run on device tensors for the per-config steps)
+    plants exactly what the seeded host recipe plants (checked here on CPU
+    tensors)."""
+    import torch
+    from oracle import topology as otopo
+    for name, B in (("sweep", 3), ("33b", 1)):
+        c = wl.config(name, B=B, V=500)
+        for t in (otopo.greedy(otopo.synthetic_accuracy(4, 10), 64), otopo.dense([4, 4, 4, 4], 256)):
+            logits = wl.base_logits(c, t.n_nodes)
+            tokens = wl.random_tokens(c, t.n_nodes)
+            ref = wl.plant(c, logits, tokens, t.parent)
+            got = torch.from_numpy(logits.copy())
+            bench.plant_on_device(c, got, torch.from_numpy(tokens), np.asarray(t.parent))
+            np.testing.assert_array_equal(got.numpy(), ref)

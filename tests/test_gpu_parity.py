@@ -304,7 +304,7 @@ def _accept_case(mg, c, t, tokens, logits, T, eps, delta):
     assert err < ACCEPT_BAND, err
     compared, flagged, differs = check_accept(al, pn, nt, logits, ref, t.parent, T, t.max_depth)
     assert compared == tokens.shape[0]
-    return ref, flagged
+    return ref, flagged, differs
 
 
 @pytest.mark.parametrize("T,eps,delta,prob", [(0.0, 0.09, 0.3, 0.6), (0.7, 0.09, 0.3, 0.6), (1.0, 0.25, 0.5, 0.5),
@@ -314,8 +314,11 @@ def test_typical_accept_parity(mg, T, eps, delta, prob):
     t = otopo.greedy(otopo.synthetic_accuracy(4, 10), 64)
     tokens = wl.random_tokens(c, t.n_nodes)
     logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=prob)
-    ref, flagged = _accept_case(mg, c, t, tokens, logits, T, eps, delta)
-    assert flagged <= 1
+    # rows with tests inside the flag band (eps = 0 puts every token with p < 1e-6
+    # there) are checked against every outcome those tests allow; at most one
+    # row may take another valid outcome than the oracle's
+    ref, flagged, differs = _accept_case(mg, c, t, tokens, logits, T, eps, delta)
+    assert differs <= 1
 
 
 def test_typical_accept_tiny_config_and_dense_tree(mg):
@@ -323,7 +326,7 @@ def test_typical_accept_tiny_config_and_dense_tree(mg):
     t = otopo.dense([2, 2])
     tokens = wl.random_tokens(c, t.n_nodes)
     logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=1.0)
-    ref, _ = _accept_case(mg, c, t, tokens, logits, 0.0, c["eps"], c["delta"])
+    ref, _, _ = _accept_case(mg, c, t, tokens, logits, 0.0, c["eps"], c["delta"])
     assert ref["accept_len"][0] == 3  # planted with probability 1 along first children
     t = otopo.dense([4, 4, 4, 4], 256)
     c = wl.config("tiny", V=3001, B=3)
