@@ -140,15 +140,11 @@ def run_ours(args, c):
 
     topo = mg.Topology.greedy(np.array(wl.synthetic_accuracy(c["K"], c["tree"][1])), c["tree"][2])
     N = topo.n_nodes
-    tdev = lambda a: _to_dev(a, dev)  # noqa: E731
     if args.profile:
-        # profiler runs: the same distributions drawn on the device (any batch fits)
-        inp = None
-        d = device_step_inputs(c, N, dev)
-    else:
-        inp = make_inputs(c, N)
-        d = {k: tdev(inp[k]) for k in ("h", "w1", "w2", "root_tok", "prefix_len", "q", "kc", "vc", "kt", "vt",
-                                       "logits")}
+        return run_profile(args, c, mg, topo, dev)
+    tdev = lambda a: _to_dev(a, dev)  # noqa: E731
+    inp = make_inputs(c, N)
+    d = {k: tdev(inp[k]) for k in ("h", "w1", "w2", "root_tok", "prefix_len", "q", "kc", "vc", "kt", "vt", "logits")}
     vs = VerifyStep(B=c["B"], H=c["H"], V=c["V"], K=c["K"], topk=c["topk"], nl=c["nl"], Hq=c["Hq"], Hkv=c["Hkv"],
                     d=c["d"], Lmax=c["Lmax"], dtype=torch.bfloat16, topology=topo, temperature=c["T"],
                     eps=c["eps"], delta=c["delta"], device=dev)
@@ -157,12 +153,9 @@ def run_ours(args, c):
     vs.heads(d["h"], d["w1"], d["w2"])
     vs.tree(d["root_tok"], d["prefix_len"])
     torch.cuda.synchronize()
-    if inp is None:
-        plant_on_device(c, d["logits"], vs.tokens, np.asarray(topo.parent))
-    else:
-        tokens = vs.tokens.cpu().numpy()
-        inp["logits"] = wl.plant(c, inp["logits"], tokens, topo.parent)
-        d["logits"] = tdev(inp["logits"])
+    tokens = vs.tokens.cpu().numpy()
+    inp["logits"] = wl.plant(c, inp["logits"], tokens, topo.parent)
+    d["logits"] = tdev(inp["logits"])
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -174,27 +167,6 @@ def run_ours(args, c):
     torch.cuda.synchronize()
     if vs.check() != 0:
         raise RuntimeError("device status set during warm-up")
-    if args.profile:
-        # Only the named call, `steps` times (for profiler captures; prints no bench line).
-        call = {"heads": lambda: vs.heads(d["h"], d["w1"], d["w2"], stream),
-                "attention": lambda: vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"],
-                                                  stream),
-                "accept": lambda: vs.accept(d["logits"], stream),
-                "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}.get(args.profile)
-        if args.profile == "linear":  # the 8-layer verify pass (807 MB of weights) at 64 tree tokens
-            lp = LinearPass(mg, c, dev)
-            lp.tokens(64)
-            call = lambda: lp.run(stream)  # noqa: E731
-        if args.profile == "head_loss":  # one sequence of 512 tokens: 262 MB of logits (above L2)
-            lc, z, y = loss_inputs(dev, "f32", B=1, S=512)
-            gz = torch.empty_like(z)
-            call = lambda: mg.medusa_head_loss(z, y, lc["decay"], dlogits=gz, stream=stream)  # noqa: E731
-        for _ in range(args.steps):
-            call()
-        torch.cuda.synchronize()
-        print(f"profile {args.profile}: {args.steps} calls done")
-        return
-
     # The whole step as one CUDA graph (the five calls are stream-ordered with no
     # host synchronisation, so they capture as they are).
     graph = vs.capture(d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"],
@@ -302,6 +274,46 @@ def run_ours(args, c):
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_profile(args, c, mg, topo, dev):
+    """Only the named call, `warmup` times and then `steps` times, on inputs
+    drawn on the device (the per-layer tensors only when the call reads them),
+    for profiler captures; prints no bench line.  Launches before the profiled
+    calls: one heads call and one packing call (set-up), then `warmup` calls."""
+    import torch
+    from medusa_head_speculative_heads_gb300.step import VerifyStep
+    N = topo.n_nodes
+    stream = torch.cuda.current_stream(dev)
+    call = None
+    if args.profile == "linear":  # the 8-layer verify pass (807 MB of weights) at 64 tree tokens
+        lp = LinearPass(mg, c, dev)
+        lp.tokens(64)
+        call = lambda: lp.run(stream)  # noqa: E731
+    elif args.profile == "head_loss":  # one sequence of 512 tokens: 262 MB of logits (above L2)
+        lc, z, y = loss_inputs(dev, "f32", B=1, S=512)
+        gz = torch.empty_like(z)
+        call = lambda: mg.medusa_head_loss(z, y, lc["decay"], dlogits=gz, stream=stream)  # noqa: E731
+    else:
+        d = device_step_inputs(c, N, dev, layers=args.profile in ("attention", "rope"))
+        vs = VerifyStep(B=c["B"], H=c["H"], V=c["V"], K=c["K"], topk=c["topk"], nl=c["nl"], Hq=c["Hq"],
+                        Hkv=c["Hkv"], d=c["d"], Lmax=c["Lmax"], dtype=torch.bfloat16, topology=topo,
+                        temperature=c["T"], eps=c["eps"], delta=c["delta"], device=dev)
+        vs.heads(d["h"], d["w1"], d["w2"], stream)
+        vs.tree(d["root_tok"], d["prefix_len"], stream)
+        torch.cuda.synchronize()
+        plant_on_device(c, d["logits"], vs.tokens, np.asarray(topo.parent))
+        call = {"heads": lambda: vs.heads(d["h"], d["w1"], d["w2"], stream),
+                "attention": lambda: vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"],
+                                                  stream),
+                "accept": lambda: vs.accept(d["logits"], stream),
+                "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}[args.profile]
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    if args.profile not in ("linear", "head_loss") and vs.check() != 0:
+        raise RuntimeError("device status set")
+    print(f"profile {args.profile}: {args.warmup} + {args.steps} calls done")
 
 
 def _capture(fn):
@@ -539,7 +551,7 @@ def lib_topology(mg, c, which="tree"):
     return mg.Topology.greedy(np.array(wl.synthetic_accuracy(c["K"], spec[1])), spec[2])
 
 
-def device_step_inputs(c, N, dev):
+def device_step_inputs(c, N, dev, layers=True):
     """The workload's per-step inputs drawn on the device from a generator seeded
     with the configuration id (same distributions as the seeded host recipe:
     h, q, K, V ~ N(0, 1), weights ~ N(0, 0.02) in bf16, base logits ~ N(0, 2)
@@ -562,7 +574,7 @@ def device_step_inputs(c, N, dev):
         normal((V, H), 0.02, d["w2"][k])
     shapes = {"q": (B, N, c["Hq"], c["d"]), "kc": (B, c["Lmax"], c["Hkv"], c["d"]),
               "vc": (B, c["Lmax"], c["Hkv"], c["d"]), "kt": (B, N, c["Hkv"], c["d"]), "vt": (B, N, c["Hkv"], c["d"])}
-    for name, shp in shapes.items():
+    for name, shp in (shapes.items() if layers else ()):
         d[name] = torch.empty((nl,) + shp, dtype=bf, device=dev)
         for l in range(nl):
             normal(shp, 1.0, d[name][l])
