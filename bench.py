@@ -630,6 +630,7 @@ def time_configs(mg, stream, dev, steps, names=None):
         if names and key not in names:
             continue
         c = wl.config(name, **({} if B is None else {"B": B}))
+        print(f"bench: workload {key}", file=sys.stderr, flush=True)
         topo = lib_topology(mg, c, which)
         N = topo.n_nodes
         d = device_step_inputs(c, N, dev)
@@ -639,6 +640,8 @@ def time_configs(mg, stream, dev, steps, names=None):
         vs.heads(d["h"], d["w1"], d["w2"], stream)
         vs.tree(d["root_tok"], d["prefix_len"], stream)
         torch.cuda.synchronize()
+        if vs.check() != 0 or not bool(((vs.tokens >= 0) & (vs.tokens < c["V"])).all()):
+            raise RuntimeError(f"{key}: tree tokens outside the vocabulary")
         plant_on_device(c, d["logits"], vs.tokens, np.asarray(topo.parent))
         args = (d["h"], d["w1"], d["w2"], d["root_tok"], d["prefix_len"], d["q"], d["kc"], d["vc"], d["kt"], d["vt"],
                 d["logits"])
@@ -857,9 +860,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--profile", choices=["heads", "attention", "accept", "rope", "linear", "head_loss"], default=None,
                     help="run only this call `steps` times after warm-up (profiler captures)")
-    ap.add_argument("--configs", default="all",
-                    help="other workloads timed as whole steps after the headline one: all, none, or a comma list of "
-                         + ", ".join(k for k, *_ in CONFIG_RUNS))
+    ap.add_argument("--configs", default="none",
+                    help="other workloads timed as whole steps after the headline one: none (default), all, or a "
+                         "comma list of " + ", ".join(k for k, *_ in CONFIG_RUNS))
     ap.add_argument("--profile-nodes", type=int, default=None,
                     help="with --profile: a greedy sparse tree of this many nodes instead of 64")
     ap.add_argument("--profile-batch", type=int, default=None,

@@ -322,9 +322,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mma_bf16(tmem + sb * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
                          kIdescQK, kk > 0);
               }
-              mma_commit(&bars->s_full[sb]);
+              // Releases first: the arrive a consumer waits for comes last.
               mma_commit(&bars->empty[slot_of<kSlots>(ck)]);
               if (j == x.T - 1) mma_commit(&bars->q_empty);
+              mma_commit(&bars->s_full[sb]);
             }
             __syncwarp();
           }
@@ -359,8 +360,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mma_bf16_ts(tmem + kColO, pa + 8 * kk, smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
                             (kk > 0 || t > 0) ? 1u : 0u);
               }
-              mma_commit(&bars->pv_done[gt & 1]);
               mma_commit(&bars->empty[slot_of<kSlots>(cv)]);
+              mma_commit(&bars->pv_done[gt & 1]);
             }
             __syncwarp();
           }
@@ -369,8 +370,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       g = g0 + x.T;
       ++n;
     }
-    if (!alive && lane == 0) {
-      // Wait (bounded) for this warp's own MMAs before TMEM is released.
+    if (lane == 0) {
+      // Wait (bounded) for this warp's own MMAs and the arrives they signal
+      // before TMEM is released and the CTA's shared memory goes away.
       uint64_t* d = s_role ? &bars->drain : &bars->drain_pv;
       mma_commit(d);
       mbar_wait_bounded(d, 0, nullptr, kDrainNs);
@@ -472,12 +474,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const bool tree = t >= x.n_pre;
         const int j0 = (tree ? t - x.n_pre : t) * p.KT + koff;  // key of s[0]
         const float sc = p.scale_log2;
-        // Raw-score maximum over the visible keys (scale > 0 keeps the order).
-        float mx = -INFINITY;
+        // Raw-score maximum over the visible keys (scale > 0 keeps the order),
+        // in four independent chains.
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (!tree && j0 + NC <= x.L && row_ok) {
           // keys entirely inside the prefix: every one is visible
 #pragma unroll
-          for (int c = 0; c < NC; ++c) mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < NC; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
         } else {
           uint32_t mw[NC / 32];
 #pragma unroll
@@ -490,9 +493,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int j = j0 + c;
             const bool v = row_ok && (tree ? (j < p.N && ((mw[c >> 5] >> (c & 31)) & 1u)) : (j < x.L));
             s[c] = v ? s[c] : -INFINITY;
-            mx = fmaxf(mx, s[c]);
+            m4[c & 3] = fmaxf(m4[c & 3], s[c]);
           }
         }
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         if constexpr (SPLIT == 2) {
           // both halves of the row continue with the maximum over all its keys
           s_mx[sb][half][m] = mx;
@@ -505,17 +509,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const float f = need ? fast_exp2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
         if (need) m_used = m_new;
         // Probabilities first (overlaps the previous tile's PV), packed to bf16.
-        // exp2(-inf) = 0 covers the masked keys.
-        float rs = 0.f;
+        // exp2(-inf) = 0 covers the masked keys.  m_used is -inf only when
+        // every score so far (this tile's included) is masked: the offset is
+        // then 0, so each exp2 sees -inf and gives 0.
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[NC / 2];
-        const float neg = -m_used;
+        const float neg = m_used == -INFINITY ? 0.f : -m_used;
 #pragma unroll
         for (int c = 0; c < NC; c += 2) {
-          const float a = m_used == -INFINITY ? 0.f : fast_exp2(fmaf(s[c], sc, neg));
-          const float b2 = m_used == -INFINITY ? 0.f : fast_exp2(fmaf(s[c + 1], sc, neg));
-          rs += a + b2;
+          const float a = fast_exp2(fmaf(s[c], sc, neg));
+          const float b2 = fast_exp2(fmaf(s[c + 1], sc, neg));
+          rs4[(c >> 1) & 3] += a + b2;
           pk[c >> 1] = pack_bf16x2(a, b2);
         }
+        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         l = l * f + rs;
         if (t > 0 && __any_sync(0xffffffffu, need)) {
           // O is rescaled only after the previous tile's PV has landed in it.

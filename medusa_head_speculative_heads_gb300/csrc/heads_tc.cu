@@ -171,7 +171,9 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       if (lane == 0) mma_commit(&bars->acc_full[ab]);
       __syncwarp();
     }
-    if (!alive && lane == 0) {
+    if (lane == 0) {
+      // Wait (bounded) for every MMA and arrive this warp issued before TMEM
+      // is released and the CTA's shared memory goes away.
       mma_commit(&bars->drain);
       mbar_wait_bounded(&bars->drain, 0, nullptr, kDrainNs);
     }
