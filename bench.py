@@ -308,12 +308,25 @@ def run_profile(args, c, mg, topo, dev):
                                                   stream),
                 "accept": lambda: vs.accept(d["logits"], stream),
                 "rope": lambda: mg.medusa_tree_rope(d["q"], d["kt"], vs.pos, stream=stream)}[args.profile]
-    for _ in range(args.warmup + args.steps):
+    for _ in range(args.warmup):
         call()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
     torch.cuda.synchronize()
     if args.profile not in ("linear", "head_loss") and vs.check() != 0:
         raise RuntimeError("device status set")
-    print(f"profile {args.profile}: {args.warmup} + {args.steps} calls done")
+    us = a.elapsed_time(b) / args.steps * 1e3
+    line = {"profile": args.profile, "workload": f"{c['name']} B={c['B']} nodes={N}", "calls": args.steps,
+            "us_per_call": round(us, 2)}
+    if args.profile in ("heads", "attention"):
+        hbm, tflops, _ = _peaks()
+        nbytes = algorithmic_bytes(c, N)[args.profile]
+        line["gbs"] = round(nbytes / us / 1e3, 1)
+        line["hbm_frac"] = round(nbytes / us / 1e3 / hbm, 4)
+    print(json.dumps(line))
 
 
 def _capture(fn):

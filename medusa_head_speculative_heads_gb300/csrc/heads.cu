@@ -399,11 +399,172 @@ topk_block_kernel(const float* __restrict__ x, const int* __restrict__ x_idx, in
   }
 }
 
+// One CTA per row: the best `topk` (<= kRowTopkMax) of n logits, ranked
+// (value desc, index asc), in two passes over the row with few divergent
+// branches.
+//  1. Every thread takes the best of its values; the topk-th best of these
+//     thread maxima (found by one warp), T, is a lower bound for the row's topk-th best (at least
+//     topk distinct values, the maxima ranked at or ahead of T, rank at or
+//     ahead of T), so every one of the row's best topk ranks at or ahead of T.
+//  2. The row is read again (from L1/L2) and the values ranked at or ahead of
+//     T, typically a few dozen, are appended to shared memory.
+//  3. topk rounds of a warp argmax over those candidates, each taking the
+//     best one ranked behind the previous round's winner, give the result in
+//     order.  Should more candidates than fit rank at or ahead of T, the
+//     rounds scan the whole row with the whole block instead (exact, slower).
+// Grid rows; out[row][topk].
+constexpr int kRowThreads = 256;
+constexpr int kRowCap = 2048;  // candidates kept in shared memory
+
+// Warp-wide best (value, index) of the lanes' arguments; every lane gets it.
+__device__ __forceinline__ void warp_best(float& v, int& id) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, id, o);
+    if (ranks_ahead(v2, i2, v, id)) { v = v2; id = i2; }
+  }
+}
+
+// Block-wide best (value, index) of the threads' arguments; every thread gets it.
+__device__ __forceinline__ void block_best(float& v, int& id, float* sv, int* si) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_best(v, id);
+  if (lane == 0) { sv[warp] = v; si[warp] = id; }
+  __syncthreads();
+  v = sv[0];
+  id = si[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+    if (ranks_ahead(sv[w], si[w], v, id)) { v = sv[w]; id = si[w]; }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+topk_rows_kernel(const float* __restrict__ x, int n, int topk, float* __restrict__ out_v, int* __restrict__ out_i) {
+  __shared__ float cv[kRowCap];
+  __shared__ int ci[kRowCap];
+  __shared__ float sv[kRowThreads / 32];
+  __shared__ int si[kRowThreads / 32];
+  __shared__ int s_count;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const float* xr = x + (size_t)row * n;
+  const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15u) == 0;
+  const int n4 = n >> 2;
+  // Visits every (value, index) of this thread's share of the row.
+  auto scan = [&](auto&& f) {
+    if (vec) {
+      const float4* x4 = reinterpret_cast<const float4*>(xr);
+      constexpr int U = 4;
+      for (int q0 = tid; q0 < n4; q0 += kRowThreads * U) {
+        float4 t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int q = q0 + u * kRowThreads;
+          if (q < n4) t[u] = x4[q];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int q = q0 + u * kRowThreads;
+          if (q < n4) {
+            f(t[u].x, 4 * q);
+            f(t[u].y, 4 * q + 1);
+            f(t[u].z, 4 * q + 2);
+            f(t[u].w, 4 * q + 3);
+          }
+        }
+      }
+    } else {
+      for (int i = tid; i < n; i += kRowThreads) f(xr[i], i);
+    }
+  };
+  // 1. thread maxima, then the topk-th best of them (warp 0 alone)
+  float mv = -INFINITY;
+  int mi = INT_MAX;
+  scan([&](float v, int i) {
+    if (ranks_ahead(v, i, mv, mi)) { mv = v; mi = i; }
+  });
+  cv[tid] = mv;
+  ci[tid] = mi;
+  __syncthreads();
+  if (tid < 32) {
+    float pv = INFINITY;
+    int pi = -1;
+    for (int r = 0; r < topk; ++r) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int j = tid; j < kRowThreads; j += 32)
+        if (ranks_ahead(pv, pi, cv[j], ci[j]) && ranks_ahead(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
+      warp_best(bv, bi);
+      pv = bv;
+      pi = bi;
+    }
+    if (tid == 0) { sv[0] = pv; si[0] = pi; s_count = 0; }
+  }
+  __syncthreads();
+  const float tv = sv[0];
+  const int ti = si[0];
+  // 2. candidates ranked at or ahead of (tv, ti)
+  scan([&](float v, int i) {
+    if (!ranks_ahead(tv, ti, v, i)) {
+      const int slot = atomicAdd(&s_count, 1);
+      if (slot < kRowCap) { cv[slot] = v; ci[slot] = i; }
+    }
+  });
+  __syncthreads();
+  const int c = s_count;
+  // 3. topk rounds, each the best candidate ranked behind the previous winner
+  // (warp 0 over the shared-memory candidates; the whole block over the row
+  // when they did not fit)
+  float pv = INFINITY;
+  int pi = -1;
+  if (c <= kRowCap) {
+    if (tid < 32) {
+      for (int r = 0; r < topk; ++r) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int j = tid; j < c; j += 32)
+          if (ranks_ahead(pv, pi, cv[j], ci[j]) && ranks_ahead(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
+        warp_best(bv, bi);
+        if (tid == 0) {
+          out_v[(size_t)row * topk + r] = bv;
+          out_i[(size_t)row * topk + r] = bi;
+        }
+        pv = bv;
+        pi = bi;
+      }
+    }
+    return;
+  }
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    scan([&](float v, int i) {
+      if (ranks_ahead(pv, pi, v, i) && ranks_ahead(v, i, bv, bi)) { bv = v; bi = i; }
+    });
+    block_best(bv, bi, sv, si);
+    if (tid == 0) {
+      out_v[(size_t)row * topk + r] = bv;
+      out_i[(size_t)row * topk + r] = bi;
+    }
+    pv = bv;
+    pi = bi;
+  }
+}
+
+constexpr int kRowTopkMax = 32;  // topk the row kernel ranks
+
 // Ranks `rows` rows of n pairs.  More than one chunk per row goes through the
 // candidate buffers (rows x chunks x topk) and one more pass, which the
 // callers size so that it fits a single chunk.
 static medusa_status launch_topk(const float* x, const int* x_idx, int rows, int n, int topk, float* cand_val,
                                  int* cand_idx, float* out_val, int* out_idx, cudaStream_t s) {
+  if (!x_idx && topk <= kRowTopkMax) {
+    launch_pdl(topk_rows_kernel, dim3(rows), dim3(kRowThreads), 0, s, x, n, topk, out_val, out_idx);
+    return launch_status();
+  }
   const int chunks = chunks_for(n);
   if (chunks == 1) {
     launch_pdl(topk_block_kernel, dim3(1, rows), dim3(kTopkThreads), 0, s, x, x_idx, n, 1, topk, out_val, out_idx);

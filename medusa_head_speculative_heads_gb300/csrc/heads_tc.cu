@@ -9,8 +9,8 @@
 // batch rows twice: rows 0..Bp-1 are the bf16 "hi" part of the fp32 vector and
 // rows Bp..2Bp-1 the "lo" remainder (v = hi + lo to ~2^-16), so the epilogue
 // sums D[:, b] + D[:, Bp + b] and the product keeps the fp32 vector's
-// precision.  For W1, X = h (exact in bf16: no lo part; those rows are the
-// TMA's zero fill); the W1 epilogue applies SiLU and the residual and writes u
+// precision.  For W1, X = h (exact in bf16: no lo part, so the product has Bp
+// columns); the W1 epilogue applies SiLU and the residual and writes u
 // split into hi/lo for W2.  The W2 epilogue writes the fp32 logits z, which
 // the regular top-k kernels then rank.
 //
@@ -56,7 +56,8 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
 struct Params {
-  int K, R, H, B, Bp, N;  // R rows per head, N = 2 * Bp
+  int K, R, H, B, Bp, N;  // R rows per head, N = 2 * Bp (rows of u2 per head)
+  int mma_n;              // columns of the product: N (W2: hi and lo rows), Bp (W1: h is exact in bf16)
   int tiles_per_head, tiles;
   int first;              // 1: W1 pass, 0: W2 pass
   const uint16_t* h;      // [B][H] bf16 (W1 residual)
@@ -111,6 +112,15 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   if (warp == 0 && lane == 0) {
     tma_prefetch(&tm_a);
     tma_prefetch(&tm_b);
+    // While an earlier kernel on the stream finishes, bring the weight boxes
+    // of this CTA's first ring fill into L2 (a hint with no data dependence:
+    // the loads after the dependency wait read whatever is current).
+    if ((int)blockIdx.x < p.tiles) {
+      const int tile = blockIdx.x;
+      const int k = tile / p.tiles_per_head, m0 = (tile % p.tiles_per_head) * 128;
+      const int n = kStages < p.H / 64 ? kStages : p.H / 64;
+      for (int kk = 0; kk < n; ++kk) tma_prefetch_l2_2d(&tm_a, kk * 64, k * p.R + m0);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -119,7 +129,10 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   pdl_trigger();
   const uint32_t tmem = s_tmem;
   const int ksteps = p.H / 64;
-  const uint32_t b_bytes = (uint32_t)p.N * 128;
+  const uint32_t b_bytes = (uint32_t)p.mma_n * 128;
+  // Each CTA walks the K blocks of its tiles starting at its own offset, so
+  // CTAs working in step do not all read the same vector box from L2 at once.
+  const int k_rot = (int)((blockIdx.x * 5u) % (unsigned)ksteps);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -128,7 +141,8 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       bool alive = true;
       for (int tile = blockIdx.x; tile < p.tiles && alive; tile += gridDim.x) {
         const int k = tile / p.tiles_per_head, m0 = (tile % p.tiles_per_head) * 128;
-        for (int kk = 0; kk < ksteps; ++kk, ++g) {
+        for (int i = 0; i < ksteps; ++i, ++g) {
+          const int kk = i + k_rot < ksteps ? i + k_rot : i + k_rot - ksteps;
           const int s = g % kStages;
           if (g >= kStages &&
               !(alive = mbar_wait_bounded(&bars->empty[s], ((g / kStages) - 1) & 1, &s_abort, kWaitNs)))
@@ -145,14 +159,14 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(128, p.N, false, false);
+    const uint32_t idesc = idesc_bf16_f32(128, p.mma_n, false, false);
     int g = 0, tc = 0;
     bool alive = true;
     for (int tile = blockIdx.x; tile < p.tiles && alive; tile += gridDim.x, ++tc) {
       const int ab = tc & 1;
       if (tc >= 2 && !(alive = warp_wait(&bars->acc_empty[ab], ((tc >> 1) - 1) & 1, &s_abort))) break;
       tc_fence_after();
-      for (int kk = 0; kk < ksteps; ++kk, ++g) {
+      for (int i = 0; i < ksteps; ++i, ++g) {
         const int s = g % kStages;
         if (!(alive = warp_wait(&bars->full[s], (g / kStages) & 1, &s_abort))) break;
         tc_fence_after();
@@ -162,7 +176,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             mma_bf16(tmem + ab * 128, smem_desc_sw128(a + j * 32, 16, 1024), smem_desc_sw128(b + j * 32, 16, 1024),
-                     idesc, (kk > 0 || j > 0) ? 1u : 0u);
+                     idesc, (i > 0 || j > 0) ? 1u : 0u);
           mma_commit(&bars->empty[s]);
         }
         __syncwarp();
@@ -197,9 +211,15 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       }
       if (!warp_wait(&bars->acc_full[ab], (tc >> 1) & 1, &s_abort)) break;
       tc_fence_after();
+      // W1 products have BP columns (no lo part), W2 products 2 BP.
       float v[NC];
+      if (p.first) {
 #pragma unroll
-      for (int c = 0; c < NC / 32; ++c) tmem_ld32(lane_addr + ab * 128 + c * 32, v + c * 32);
+        for (int c = 0; c < BP / 8; ++c) tmem_ld8(lane_addr + ab * 128 + c * 8, v + c * 8);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c) tmem_ld32(lane_addr + ab * 128 + c * 32, v + c * 32);
+      }
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[ab]);
@@ -207,7 +227,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       if (row >= p.R) continue;
 #pragma unroll
       for (int b = 0; b < BP; ++b) {
-        const float zsum = v[b] + v[BP + b];
+        const float zsum = p.first ? v[b] : v[b] + v[BP + b];
         if (p.first) {
           float val = 0.f;
           if (b < p.B) val = zsum / (1.f + expf(-zsum)) + bf16_bits_to_f32((hres[b >> 1] >> (16 * (b & 1))) & 0xffffu);
@@ -273,7 +293,7 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
                            uint16_t* u2, float* z, int32_t* d_status, cudaStream_t s) {
   const int Bp = heads_tc_bp(B), N = 2 * Bp;
   CUtensorMap ma1, mb1, ma2, mb2;
-  if (!map_rows(&ma1, w1, H, (long long)K * H, 128) || !map_rows(&mb1, h, H, B, N) ||
+  if (!map_rows(&ma1, w1, H, (long long)K * H, 128) || !map_rows(&mb1, h, H, B, Bp) ||
       !map_rows(&ma2, w2, H, (long long)K * V, 128) || !map_rows(&mb2, u2, H, (long long)K * N, N))
     return MEDUSA_ERR_CUDA;
   auto kern = Bp == 16 ? heads_tc_kernel<16> : Bp == 32 ? heads_tc_kernel<32> : Bp == 48 ? heads_tc_kernel<48>
@@ -303,12 +323,14 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   // W1: rows per head = H
   p.R = H;
   p.first = 1;
+  p.mma_n = Bp;
   p.tiles_per_head = ceil_div(H, 128);
   p.tiles = K * p.tiles_per_head;
   launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma1, mb1, p);
   // W2: rows per head = V
   p.R = V;
   p.first = 0;
+  p.mma_n = N;
   p.tiles_per_head = ceil_div(V, 128);
   p.tiles = K * p.tiles_per_head;
   launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma2, mb2, p);

@@ -99,6 +99,28 @@ def test_head_topk_bit_exact(mg, V, topk):
     np.testing.assert_array_equal(to_host(val).astype(np.float64), ref_val)
 
 
+def test_head_topk_when_the_best_values_crowd_a_few_threads(mg):
+    """Rows whose best values all sit in the shares of 32 of the ranking kernel's
+    256 threads (every 256th group of four columns, offsets 0-31): more than
+    its shared-memory candidate list holds rank ahead of the threshold, so the
+    rounds scan the whole row.  Bit-exact against the oracle, with ties."""
+    g = np.random.default_rng(7)
+    V = 32000
+    x = (np.round(g.standard_normal((3, V)) * 8) / 8).astype(np.float32)
+    cols = np.arange(V)
+    owner = (cols // 4) % 256
+    crowd = owner < 31  # 31 shares of large values, rounded (ties)
+    x[:, crowd] = np.round(2000 + 1000 * g.random((3, int(crowd.sum()))), 1)
+    low = owner == 31   # the 32nd share peaks lower: the 32nd-best maximum sits below ~3900 values
+    x[:, low] = np.round(1000 + 500 * g.random((3, int(low.sum()))), 1)
+    for topk in (32, 16):
+        ref_idx, ref_val = oracle.topk_f32(x, topk)
+        idx, val = mg.medusa_head_topk(to_dev(x), topk)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_host(idx), ref_idx)
+        np.testing.assert_array_equal(to_host(val).astype(np.float64), ref_val)
+
+
 # ----------------------------------------------------------------------------- tree build
 
 @pytest.mark.parametrize("kind", ["dense7", "dense256", "greedy64", "choices", "chain", "root_only"])
