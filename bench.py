@@ -880,16 +880,22 @@ def main():
                     help="with --profile: a greedy sparse tree of this many nodes instead of 64")
     ap.add_argument("--profile-batch", type=int, default=None,
                     help="with --profile: the 7B-shape batch-sweep workload at this batch instead of batch 1")
+    ap.add_argument("--profile-shape", default=None,
+                    help="with --profile: layers,q_heads,kv_heads,prefix of the workload (e.g. 1,8,2,32768: few "
+                         "items with a long prefix)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if (args.profile_nodes is not None or args.profile_batch is not None) and not args.profile:
-        ap.error("--profile-nodes / --profile-batch apply to --profile runs only")
+    if (args.profile_nodes is not None or args.profile_batch is not None or args.profile_shape) and not args.profile:
+        ap.error("--profile-nodes / --profile-batch / --profile-shape apply to --profile runs only")
     c = wl.config("7b")
     if args.profile_batch is not None:
         c = wl.config("sweep", B=args.profile_batch)
     if args.profile_nodes is not None:
         c = wl.config(c["name"], B=c["B"], tree=(c["tree"][0], c["tree"][1], args.profile_nodes))
+    if args.profile_shape:
+        nl, hq, hkv, L = (int(v) for v in args.profile_shape.split(","))
+        c = wl.config(c["name"], B=c["B"], tree=c["tree"], nl=nl, Hq=hq, Hkv=hkv, L=L)
     if args.impl == "reference":
         run_reference(args, c)
     else:

@@ -195,7 +195,14 @@ medusa_status medusa_tree_build(const medusa_dev_topology* t, const int32_t* roo
  * never uses TF32).  Cache rows at and past prefix_len[b] are never read into
  * the result.  prefix_len outside [0, Lmax] sets BAD_LENGTH and the row's
  * output is left unwritten.  Limits: N <= MEDUSA_MAX_NODES, d a multiple of 32,
- * d <= 256, Hq a multiple of Hkv, pointers 16-byte aligned. */
+ * d <= 256, Hq a multiple of Hkv, pointers 16-byte aligned.
+ * Split key ranges: the tensor-core kernel runs whole (layer, row, kv-head
+ * group) items in full rounds over the SMs; when the last round would leave
+ * SMs idle, each of its items is split into key-range pieces whose partial
+ * results (unnormalised O, row maximum, row sum) are merged by a second kernel
+ * in the same call (online-softmax rescaling).  The partials need
+ * medusa_tree_attention_workspace_size() bytes of 16-byte aligned workspace
+ * (0 when no split is planned for these sizes on the current device). */
 size_t medusa_tree_attention_workspace_size(int n_layers, int B, int N, int Hq, int Hkv, int d,
                                             int Lmax, medusa_dtype dt);
 medusa_status medusa_tree_attention(const void* q, const void* kc, const void* vc, const void* kt,

@@ -88,6 +88,11 @@ struct Params {
   int mtiles;    // row tiles per head group
   int groups;    // head groups per (layer, row)
   int items;
+  int units;       // work units: the first full_items items whole, then each remaining item in `pieces` parts
+  int full_items;
+  int pieces;      // key-range pieces per remaining item (1: nothing is split)
+  float* part_o;   // [piece][128 rows][128] fp32 unnormalised O of each piece
+  float* part_ml;  // [piece][128 rows][2] fp32 row maximum (log2 domain) and row sum of each piece
   int KT;        // key positions per tile: 64 packed, 128 otherwise
   int out32;     // output base 32-byte aligned (32-byte stores)
   float scale_log2;
@@ -160,6 +165,46 @@ __device__ __forceinline__ Item decode(const Params& p, int it) {
   return x;
 }
 
+// A work unit: a whole item (piece -1), or key tiles [t0, t1) of one of the
+// items after the first full_items, whose partial result goes to slot `piece`.
+struct Unit {
+  Item x;
+  int t0, t1, piece;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+  Unit w;
+  if (u < p.full_items) {
+    w.x = decode(p, u);
+    w.t0 = 0;
+    w.t1 = w.x.T;
+    w.piece = -1;
+  } else {
+    const int v = u - p.full_items, s = v % p.pieces;
+    w.x = decode(p, p.full_items + v / p.pieces);
+    w.t0 = s * w.x.T / p.pieces;
+    w.t1 = (s + 1) * w.x.T / p.pieces;
+    w.piece = v;
+  }
+  return w;
+}
+
+// Output row of tile row m of an item: (node, query head) and whether it exists.
+struct RowTarget {
+  int node, h, gq;
+  bool ok;
+};
+__device__ __forceinline__ RowTarget row_target(const Params& p, const Item& x, int m) {
+  RowTarget r;
+  int rr;
+  if (p.packed) { rr = m & 63; r.h = x.h0 + (m >> 6); }
+  else { rr = x.mt * 128 + m; r.h = x.h0; }
+  r.node = rr / p.G;
+  r.gq = rr % p.G;
+  r.ok = r.node < p.N && r.h < p.Hkv;
+  return r;
+}
+
 }  // namespace tc
 
 template <bool PACKED, int SPLIT>
@@ -216,8 +261,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // on the stream finishes, warm L2 with the first two K and V tiles of this
     // CTA's first item (rows 0 .. 2 KT of its cache, whatever its length; the
     // item's row and heads come from the launch alone).
-    if ((int)blockIdx.x < p.items) {
-      const int r = (int)blockIdx.x / p.mtiles;
+    if ((int)blockIdx.x < p.units) {
+      const int first_item = (int)blockIdx.x < p.full_items
+                                 ? (int)blockIdx.x
+                                 : p.full_items + ((int)blockIdx.x - p.full_items) / p.pieces;
+      const int r = first_item / p.mtiles;
       const int lb = r / p.groups, h0 = p.packed ? 2 * (r % p.groups) : r % p.groups;
       for (int t = 0; t < 2; ++t)
         for (int kv = 0; kv < 2; ++kv)
@@ -240,9 +288,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (lane == 0) {
       int g = 0, n = 0, issued = 0;
       bool alive = true;
-      for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
-        const Item x = decode(p, it);
-        if (!x.ok) continue;
+      for (int u = blockIdx.x; u < p.units && alive; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        const Item& x = w.x;
+        if (!x.ok || w.t1 <= w.t0) continue;
         if (n > 0 && !(alive = mbar_wait_bounded(&bars->q_empty, (n - 1) & 1, &s_abort, kWaitNs))) break;
         ++n;  // Q loads of item n-1 (0-based) issued below
         mbar_expect_tx(&bars->q_full, 2 * kHalf);
@@ -254,11 +303,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tma_load_5d(smem + kOffQ + dh * kHalf, &tm_q, &bars->q_full, 64 * dh, 0, x.h0, x.mt * (128 / p.G), x.lb);
           }
         }
-        int c = 2 * g;  // half-tiles of earlier items: 2T each
-        for (int j = 0; j < x.T + kLag && alive; ++j) {
+        int c = 2 * g;  // half-tiles of earlier units: two per tile
+        const int cnt = w.t1 - w.t0;
+        for (int j = 0; j < cnt + kLag && alive; ++j) {
           for (int kv = 0; kv < 2 && alive; ++kv) {
-            const int t = kv ? j - kLag : j;  // K(j), then V(j - kLag)
-            if (t < 0 || t >= x.T) continue;
+            const int tt = kv ? j - kLag : j;  // K(j), then V(j - kLag), relative to t0
+            if (tt < 0 || tt >= cnt) continue;
+            const int t = w.t0 + tt;
             const bool tree = t >= x.n_pre;
             const int j0 = (tree ? t - x.n_pre : t) * p.KT;
             const int sl = slot_of<kSlots>(c);
@@ -275,7 +326,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             issued = ++c;
           }
         }
-        g += x.T;
+        g += cnt;
       }
       if (!alive) {
         // Drain: wait (bounded, regardless of the abort flag) for the last
@@ -294,20 +345,23 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const bool s_role = warp == 1;
     int g = 0, n = 0;
     bool alive = true;
-    for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
-      const Item x = decode(p, it);
+    for (int u = blockIdx.x; u < p.units && alive; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      const Item& x = w.x;
       if (!x.ok) {
-        if (s_role && lane == 0 && x.mt == 0) set_status(p.d_status, MEDUSA_DEV_BAD_LENGTH);
+        if (s_role && lane == 0 && x.mt == 0 && w.t0 == 0) set_status(p.d_status, MEDUSA_DEV_BAD_LENGTH);
         continue;
       }
+      if (w.t1 <= w.t0) continue;
+      const int cnt = w.t1 - w.t0;
       if (s_role) {
         if (!(alive = warp_wait(&bars->q_full, n & 1, &s_abort))) break;
         tc_fence_after();
       }
       const int g0 = g;
       int c = 2 * g0;  // next half-tile of the load sequence
-      for (int j = 0; j < x.T + kLag && alive; ++j) {
-        if (j < x.T) {
+      for (int j = 0; j < cnt + kLag && alive; ++j) {
+        if (j < cnt) {
           const int gj = g0 + j, ck = c++, sb = gj & 1;
           if (s_role) {
             if (!(alive = warp_wait(&bars->full[slot_of<kSlots>(ck)], use_parity<kSlots>(ck), &s_abort))) break;
@@ -324,16 +378,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               }
               // Releases first: the arrive a consumer waits for comes last.
               mma_commit(&bars->empty[slot_of<kSlots>(ck)]);
-              if (j == x.T - 1) mma_commit(&bars->q_empty);
+              if (j == cnt - 1) mma_commit(&bars->q_empty);
               mma_commit(&bars->s_full[sb]);
             }
             __syncwarp();
           }
         }
         if (j >= kLag) {
-          const int t = j - kLag, gt = g0 + t, cv = c++;
+          const int tt = j - kLag, t = w.t0 + tt, gt = g0 + tt, cv = c++;
           if (!s_role) {
-            if (t == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
+            if (tt == 0 && n > 0 && !(alive = warp_wait(&bars->o_free, (n - 1) & 1, &s_abort))) break;
             if (!(alive = warp_wait(&bars->p_full[gt & 1], (gt >> 1) & 1, &s_abort))) break;
             if (!(alive = warp_wait(&bars->full[slot_of<kSlots>(cv)], use_parity<kSlots>(cv), &s_abort))) break;
             uint8_t* vb = smem + kOffRing + slot_of<kSlots>(cv) * kSlotBytes;
@@ -358,7 +412,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 mma_bf16_ts(tmem + kColO, pa + 8 * kk, smem_desc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
-                            (kk > 0 || t > 0) ? 1u : 0u);
+                            (kk > 0 || tt > 0) ? 1u : 0u);
               }
               mma_commit(&bars->empty[slot_of<kSlots>(cv)]);
               mma_commit(&bars->pv_done[gt & 1]);
@@ -367,7 +421,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           }
         }
       }
-      g = g0 + x.T;
+      g = g0 + cnt;
       ++n;
     }
     if (lane == 0) {
@@ -406,8 +460,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // waits for o_free).
     bool pend = false, pend_ok = false;
     uint16_t* pend_row = nullptr;
-    float pend_l = 0.f;
-    int pend_g = 0;
+    float pend_l = 0.f, pend_m = 0.f;
+    int pend_g = 0, pend_piece = -1;
     auto finish = [&]() -> bool {
       float l = pend_l;
       if constexpr (SPLIT == 2) {
@@ -420,6 +474,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       ++nf;
       if (!warp_wait(&bars->pv_done[pend_g & 1], (pend_g >> 1) & 1, &s_abort)) return false;
       tc_fence_after();
+      // A piece of an item leaves its unnormalised O, row maximum and row sum
+      // for the merge kernel; a whole item writes O / l.
+      float* part = pend_piece >= 0 ? p.part_o + ((size_t)pend_piece * 128 + m) * 128 : nullptr;
+      if (pend_piece >= 0 && half == 0)
+        *reinterpret_cast<float2*>(p.part_ml + ((size_t)pend_piece * 128 + m) * 2) = make_float2(pend_m, l);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       // O in chunks of EC columns (one TMEM wait per chunk; 128-row tiles use
       // narrower chunks, their softmax already holds most registers).
@@ -430,7 +489,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
         for (int q = 0; q < EC / 32; ++q) tmem_ld32(lane_addr + kColO + OC * half + EC * h2 + 32 * q, o + 32 * q);
         tmem_wait_ld();
-        if (pend_ok) {
+        if (part) {
+          float4* dst = reinterpret_cast<float4*>(part + OC * half + EC * h2);
+#pragma unroll
+          for (int q = 0; q < EC / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        } else if (pend_ok) {
           uint32_t w[EC / 2];
 #pragma unroll
           for (int e = 0; e < EC / 2; ++e) w[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
@@ -450,9 +513,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       pend = false;
       return true;
     };
-    for (int it = blockIdx.x; it < p.items && alive; it += gridDim.x) {
-      const Item x = decode(p, it);
+    for (int u = blockIdx.x; u < p.units && alive; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      const Item& x = w.x;
       if (!x.ok) continue;
+      if (w.t1 <= w.t0) {
+        // an empty piece (an item with fewer key tiles than pieces): no keys
+        if (half == 0)
+          *reinterpret_cast<float2*>(p.part_ml + ((size_t)w.piece * 128 + m) * 2) = make_float2(-INFINITY, 0.f);
+        continue;
+      }
       // This thread's query row.
       int r, h;
       if (PACKED) { r = m & 63; h = x.h0 + slot; }
@@ -460,7 +530,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int node = r / p.G, gq = r % p.G;
       const bool row_ok = node < p.N && h < p.Hkv;
       float m_used = -INFINITY, l = 0.f;
-      for (int t = 0; t < x.T; ++t, ++g) {
+      for (int t = w.t0; t < w.t1; ++t, ++g) {
         const int sb = g & 1;
         if (!(alive = warp_wait(&bars->s_full[sb], (g >> 1) & 1, &s_abort))) break;
         tc_fence_after();
@@ -524,7 +594,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         l = l * f + rs;
-        if (t > 0 && __any_sync(0xffffffffu, need)) {
+        if (t > w.t0 && __any_sync(0xffffffffu, need)) {
           // O is rescaled only after the previous tile's PV has landed in it.
           const int gp = g - 1;
           if (!(alive = warp_wait(&bars->pv_done[gp & 1], (gp >> 1) & 1, &s_abort))) break;
@@ -557,7 +627,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_arrive(&bars->p_full[pb]);
         // The previous item's epilogue (its PV(0) waits for O to be read out).
         if constexpr (PACKED) {
-          if (t == 0 && pend && !(alive = finish())) break;
+          if (t == w.t0 && pend && !(alive = finish())) break;
         }
       }
       if (!alive) break;
@@ -565,6 +635,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       pend_ok = row_ok;
       pend_row = p.out + ((((size_t)x.lb * p.N + (row_ok ? node : 0)) * p.Hq) + (size_t)h * p.G + gq) * 128;
       pend_l = l;
+      pend_m = m_used;
+      pend_piece = w.piece;
       pend_g = g - 1;
       // 128-row tiles keep every score register live inside the tile loop:
       // their epilogue runs here, right after the item.
@@ -582,6 +654,55 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   // finished) is visible here.
   if (threadIdx.x == 0 && s_abort) set_status(p.d_status, MEDUSA_DEV_TIMEOUT);
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Merges the pieces of every split item: for each of its rows, the pieces'
+// (O, m, l) combine as in the online softmax, O = sum_s 2^(m_s - M) O_s and
+// l = sum_s 2^(m_s - M) l_s with M = max_s m_s, and the row is written as
+// O / l.  One warp per (split item, row): the lanes share the pieces for M and
+// l, then every lane adds its 4 columns of each piece's O (loads independent
+// of one another, several in flight).  Grid: split items x 16, 8 warps each.
+__global__ void __launch_bounds__(256) tree_attn_merge_kernel(const tc::Params p) {
+  using namespace tc;
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + warp;
+  const int v = gw >> 7, m = gw & 127;  // split item (0-based after the whole ones), tile row
+  if (v >= p.items - p.full_items) return;
+  const Item x = decode(p, p.full_items + v);
+  if (!x.ok) return;
+  const RowTarget rt = row_target(p, x, m);
+  if (!rt.ok) return;
+  const size_t base = (size_t)v * p.pieces;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float M = -INFINITY;
+  for (int s = lane; s < p.pieces; s += 32) {
+    const float2 q = ml[(base + s) * 128 + m];
+    if (q.y > 0.f) M = fmaxf(M, q.x);
+  }
+  M = warp_max(M);
+  float l = 0.f;
+  for (int s = lane; s < p.pieces; s += 32) {
+    const float2 q = ml[(base + s) * 128 + m];
+    if (q.y > 0.f) l = fmaf(fast_exp2(q.x - M), q.y, l);
+  }
+  l = warp_sum(l);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = 0; s < p.pieces; ++s) {
+    const size_t slot = (base + s) * 128 + m;
+    const float2 q = ml[slot];
+    const float4 po = reinterpret_cast<const float4*>(p.part_o + slot * 128)[lane];
+    const float wgt = q.y > 0.f ? fast_exp2(q.x - M) : 0.f;  // a piece with no visible key adds nothing
+    o.x = fmaf(wgt, po.x, o.x);
+    o.y = fmaf(wgt, po.y, o.y);
+    o.z = fmaf(wgt, po.z, o.z);
+    o.w = fmaf(wgt, po.w, o.w);
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint16_t* dst = p.out + ((((size_t)x.lb * p.N + rt.node) * p.Hq) + (size_t)rt.h * p.G + rt.gq) * 128 + 4 * lane;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
 }
 
 // ------------------------------------------------------------------ host side
@@ -609,6 +730,52 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// How the items are divided.  When there are fewer than half as many items as
+// SMs (few layers x rows x heads with long prefixes), each item is split into
+// `pieces` key ranges so that (nearly) every SM streams part of the cache; a
+// split needs at least two pieces per item and two key tiles per piece at the
+// cache capacity.  Otherwise every item runs whole: with a round or more of
+// items the cache stream already keeps HBM near its peak, and splitting the
+// last round only adds partial traffic and a merge (measured slower on the
+// Vicuna-7B step: 121 us instead of 101 us for the call).  The general form
+// below (whole items in full rounds, then the last round's items split) is
+// kept, with full rounds absent whenever a split happens.
+struct AttnPlan {
+  int items, full_items, pieces, units, grid;
+  bool packed;
+  size_t ws_bytes;
+};
+static AttnPlan attn_plan(int n_layers, int B, int N, int Hq, int Hkv, int Lmax, int sms) {
+  AttnPlan a{};
+  const int G = Hq / Hkv;
+  a.packed = N * G <= 64;
+  const int KT = a.packed ? 64 : 128;
+  const int mtiles = a.packed ? 1 : (N * G + 127) / 128;
+  const int groups = a.packed ? (Hkv + 1) / 2 : Hkv;
+  a.items = n_layers * B * groups * mtiles;
+  const int rem = 2 * a.items <= sms ? a.items : 0;
+  const int max_tiles = (Lmax + KT - 1) / KT + (N + KT - 1) / KT;
+  int pieces = rem > 0 ? sms / rem : 1;
+  if (pieces > max_tiles / 2) pieces = max_tiles / 2;
+  if (pieces >= 2) {
+    a.pieces = pieces;
+    a.full_items = a.items - rem;
+    a.units = a.full_items + rem * pieces;
+    a.grid = a.units < sms ? a.units : sms;
+    a.ws_bytes = (size_t)rem * pieces * 128 * (128 + 2) * sizeof(float);
+  } else {
+    // Equal-cost items: as many rounds as the SM count forces, then spread
+    // the items evenly over just enough CTAs (no ragged last round).
+    a.pieces = 1;
+    a.full_items = a.items;
+    a.units = a.items;
+    const int rounds = (a.items + sms - 1) / sms;
+    a.grid = (a.items + rounds - 1) / rounds;
+    a.ws_bytes = 0;
+  }
+  return a;
+}
+
 bool tree_attention_tc_supported(int N, int Hq, int Hkv, int d, int Lmax, const void* q, const void* kc,
                                  const void* vc, const void* kt, const void* vt, const void* out) {
   if (d != 128 || Hkv < 1 || Hq % Hkv || N < 1 || N > MEDUSA_MAX_NODES || Lmax < 1) return false;
@@ -619,14 +786,18 @@ bool tree_attention_tc_supported(int N, int Hq, int Hkv, int d, int Lmax, const 
   return encode_fn() != nullptr;
 }
 
-size_t tree_attention_tc_ws_bytes(int, int, int, int, int, int, int) { return 0; }
+size_t tree_attention_tc_ws_bytes(int n_layers, int B, int N, int Hq, int Hkv, int, int Lmax) {
+  return attn_plan(n_layers, B, N, Hq, Hkv, Lmax, device_sm_count()).ws_bytes;
+}
 
 medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, const void* kt, const void* vt,
                                 const uint32_t* mask, const int32_t* prefix_len, int n_layers, int B, int N,
-                                int Hq, int Hkv, int d, int Lmax, float scale, void* out, void*, size_t,
+                                int Hq, int Hkv, int d, int Lmax, float scale, void* out, void* ws, size_t ws_bytes,
                                 int32_t* d_status, cudaStream_t s) {
   (void)d;
   const int G = Hq / Hkv;
+  const AttnPlan plan = attn_plan(n_layers, B, N, Hq, Hkv, Lmax, device_sm_count());
+  if (plan.ws_bytes && (!ws || ws_bytes < plan.ws_bytes || !aligned16(ws))) return MEDUSA_ERR_WORKSPACE;
   tc::Params p;
   p.mask = mask;
   p.prefix_len = prefix_len;
@@ -646,6 +817,11 @@ medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, c
   p.mtiles = p.packed ? 1 : (N * G + 127) / 128;
   p.groups = p.packed ? (Hkv + 1) / 2 : Hkv;
   p.items = n_layers * B * p.groups * p.mtiles;
+  p.units = plan.units;
+  p.full_items = plan.full_items;
+  p.pieces = plan.pieces;
+  p.part_o = plan.ws_bytes ? static_cast<float*>(ws) : nullptr;
+  p.part_ml = plan.ws_bytes ? p.part_o + (size_t)(plan.items - plan.full_items) * plan.pieces * 128 * 128 : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   const cuuint64_t LB = (cuuint64_t)n_layers * B;
   const cuuint64_t es = 2;
@@ -678,12 +854,9 @@ medusa_status tree_attention_tc(const void* q, const void* kc, const void* vc, c
   const uint32_t smem = tc::smem_bytes(p.packed ? kSplitPacked : 2);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  // Equal-cost items: as many rounds as the SM count forces, then spread the
-  // items evenly over just enough CTAs (no ragged last round).
-  const int sms = device_sm_count();
-  const int rounds = (p.items + sms - 1) / sms;
-  const int grid = (p.items + rounds - 1) / rounds;
-  launch_pdl(kern, dim3(grid), dim3(threads), smem, s, mq, mkc, mvc, mkt, mvt, p);
+  launch_pdl(kern, dim3(plan.grid), dim3(threads), smem, s, mq, mkc, mvc, mkt, mvt, p);
+  if (plan.pieces > 1)
+    launch_pdl(tree_attn_merge_kernel, dim3((plan.items - plan.full_items) * 16), dim3(256), 0, s, p);
   return launch_status();
 }
 

@@ -43,8 +43,8 @@ class VerifyStep:
         self.ws_heads = B_._ws(L.medusa_heads_workspace_size(B, H, V, K, topk), device)
         self.ws_attn = B_._ws(L.medusa_tree_attention_workspace_size(nl, B, N, Hq, Hkv, d, Lmax, dt), device)
         self.ws_acc = B_._ws(L.medusa_typical_accept_workspace_size(B, N, V), device)
-        # one attention launch when the library asks for no workspace (neither path does
-        # today); a workspace would hold partials merged by a second launch
+        # one attention launch when the library asks for no workspace; a workspace holds
+        # the partials of split key ranges, merged by a second launch
         self.attn_launches = 1 if self.ws_attn is None else 2
 
     def heads(self, h, w1, w2, stream=None):

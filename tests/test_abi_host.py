@@ -189,6 +189,26 @@ def test_host_validation_rejects_before_launch():
     assert L.medusa_status_string(4) == b"MEDUSA_ERR_CUDA"
 
 
+def test_attention_workspace_follows_the_split_plan():
+    """Tree attention splits key ranges only when there are fewer than half as
+    many items as SMs (152 assumed where no GPU is visible), 128 rows x
+    (128 + 2) floats of partials per piece: four items of 128 rows split into
+    as many pieces as keep two key tiles each at the cache capacity (5 at 1088
+    rows with 9 tiles, 16 at 4064 rows, 38 = 152 / 4 at 32832 rows); 76 items
+    split in two; the Vicuna-7B shape's 512 items, 77 items or fp32 split
+    nothing."""
+    L = mg.lib()
+    bf16 = binding.MEDUSA_BF16
+    piece = 128 * 130 * 4
+    assert L.medusa_tree_attention_workspace_size(2, 1, 64, 4, 2, 128, 1088, bf16) == 4 * 5 * piece
+    assert L.medusa_tree_attention_workspace_size(1, 1, 64, 8, 2, 128, 4064, bf16) == 4 * 16 * piece
+    assert L.medusa_tree_attention_workspace_size(1, 1, 64, 8, 2, 128, 32832, bf16) == 4 * 38 * piece
+    assert L.medusa_tree_attention_workspace_size(32, 1, 64, 32, 32, 128, 1088, bf16) == 0
+    assert L.medusa_tree_attention_workspace_size(76, 1, 64, 2, 2, 128, 1088, bf16) == 76 * 2 * piece
+    assert L.medusa_tree_attention_workspace_size(77, 1, 64, 2, 2, 128, 1088, bf16) == 0
+    assert L.medusa_tree_attention_workspace_size(32, 1, 64, 32, 32, 128, 1088, binding.MEDUSA_F32) == 0
+
+
 def _linear_scratch(T, K, N, sms=152):
     """The linear layer's scratch from its stated division: tiles of 128 features
     by TN tokens, the K blocks of all tiles end to end divided over

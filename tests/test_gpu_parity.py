@@ -175,6 +175,10 @@ ATTN_CASES = [
     # more work items than SMs: every CTA runs several items through the pipeline
     dict(name="tiny", dtype="bf16", nl=4, B=2, Hq=40, Hkv=40, d=128, L=200, tree=("greedy", 10, 64),
          Ls=[200, 64]),
+    # few items with a long prefix: four 128-row items split into 16 key ranges each,
+    # merged by online softmax (the 12 items of the second case are split in three,
+    # with empty ranges for its row without a prefix)
+    dict(name="tiny", dtype="bf16", nl=1, B=1, Hq=8, Hkv=2, d=128, L=4000, tree=("greedy", 10, 64), Ls=[4000]),
 ]
 
 
