@@ -110,9 +110,9 @@ class VerifyStep:
     def launches_per_step(self) -> int:
         """Kernels the five calls launch (mirrors the library's dispatch)."""
         import torch
-        B, V = self.dims["B"], self.dims["V"]
+        B = self.dims["B"]
         if B >= 4 and self.dtype == torch.bfloat16 and self.dims["H"] % 64 == 0:
-            heads = 2 + (2 if V > 4096 else 1)  # tensor-core W1, W2, then the top-k of z
+            heads = 3  # tensor-core W1, W2, then one ranking kernel over the rows of z
         else:
             heads = 2 * (-(-B // 8))  # W1 and W2 per pass of <= 8 rows; the W2 pass merges the top-k
         attn = self.attn_launches
