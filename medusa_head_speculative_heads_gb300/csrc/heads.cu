@@ -554,7 +554,127 @@ topk_rows_kernel(const float* __restrict__ x, int n, int topk, float* __restrict
   }
 }
 
-constexpr int kRowTopkMax = 32;  // topk the row kernel ranks
+constexpr int kRowTopkMax = 32;  // topk the row kernels rank
+
+// Top-k of rows whose 32-element group maxima are known (written by the
+// tensor-core W2 epilogue): one CTA per row.
+//  1. Every thread takes the best (maximum, group) of its groups; the topk-th
+//     best of these thread bests (warp 0), value T, is at most the row's
+//     topk-th best value (topk distinct groups, hence topk distinct elements,
+//     reach T).
+//  2. Only the groups whose maximum reaches T can hold a value >= T; their
+//     elements >= T (every top-k element among them) go to shared memory.
+//  3. topk rounds of a warp argmax over those candidates, as in
+//     topk_rows_kernel, with the same whole-row fallback when they overflow.
+// Grid rows; gmax[row][groups], group g = elements [32 g, 32 g + 32).
+__global__ void __launch_bounds__(kRowThreads)
+topk_groups_kernel(const float* __restrict__ x, const float* __restrict__ gmax, int n, int groups, int topk,
+                   float* __restrict__ out_v, int* __restrict__ out_i) {
+  __shared__ float cv[kRowCap];
+  __shared__ int ci[kRowCap];
+  __shared__ float sv[kRowThreads / 32];
+  __shared__ int si[kRowThreads / 32];
+  __shared__ int s_count;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const float* xr = x + (size_t)row * n;
+  const float* gr = gmax + (size_t)row * groups;
+  // 1. thread bests over the group maxima, then the topk-th best of them
+  float mv = -INFINITY;
+  int mg = INT_MAX;
+  for (int g = tid; g < groups; g += kRowThreads) {
+    const float v = gr[g];
+    if (ranks_ahead(v, g, mv, mg)) { mv = v; mg = g; }
+  }
+  cv[tid] = mv;
+  ci[tid] = mg;
+  __syncthreads();
+  if (tid < 32) {
+    float pv = INFINITY;
+    int pi = -1;
+    for (int r = 0; r < topk; ++r) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int j = tid; j < kRowThreads; j += 32)
+        if (ranks_ahead(pv, pi, cv[j], ci[j]) && ranks_ahead(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
+      warp_best(bv, bi);
+      pv = bv;
+      pi = bi;
+    }
+    if (tid == 0) { sv[0] = pv; s_count = 0; }
+  }
+  __syncthreads();
+  const float T = sv[0];
+  // 2. elements >= T of the groups that reach T
+  const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15u) == 0;
+  for (int g = tid; g < groups; g += kRowThreads) {
+    if (!(gr[g] >= T)) continue;
+    const int e0 = 32 * g;
+    if (vec && e0 + 32 <= n) {
+      float4 t[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) t[q] = reinterpret_cast<const float4*>(xr + e0)[q];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float e[4] = {t[q].x, t[q].y, t[q].z, t[q].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (e[c] >= T) {
+            const int slot = atomicAdd(&s_count, 1);
+            if (slot < kRowCap) { cv[slot] = e[c]; ci[slot] = e0 + 4 * q + c; }
+          }
+      }
+    } else {
+      for (int i = e0; i < e0 + 32 && i < n; ++i) {
+        const float v = xr[i];
+        if (v >= T) {
+          const int slot = atomicAdd(&s_count, 1);
+          if (slot < kRowCap) { cv[slot] = v; ci[slot] = i; }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int c = s_count;
+  // 3. topk rounds, each the best candidate ranked behind the previous winner
+  float pv = INFINITY;
+  int pi = -1;
+  if (c <= kRowCap) {
+    if (tid < 32) {
+      for (int r = 0; r < topk; ++r) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int j = tid; j < c; j += 32)
+          if (ranks_ahead(pv, pi, cv[j], ci[j]) && ranks_ahead(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
+        warp_best(bv, bi);
+        if (tid == 0) {
+          out_v[(size_t)row * topk + r] = bv;
+          out_i[(size_t)row * topk + r] = bi;
+        }
+        pv = bv;
+        pi = bi;
+      }
+    }
+    return;
+  }
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int i = tid; i < n; i += kRowThreads) {
+      const float v = xr[i];
+      if (ranks_ahead(pv, pi, v, i) && ranks_ahead(v, i, bv, bi)) { bv = v; bi = i; }
+    }
+    block_best(bv, bi, sv, si);
+    if (tid == 0) {
+      out_v[(size_t)row * topk + r] = bv;
+      out_i[(size_t)row * topk + r] = bi;
+    }
+    pv = bv;
+    pi = bi;
+  }
+}
 
 // Ranks `rows` rows of n pairs.  More than one chunk per row goes through the
 // candidate buffers (rows x chunks x topk) and one more pass, which the
@@ -665,22 +785,23 @@ static size_t heads_cand2(int B, int V, int K, int topk) {
 int heads_tc_bp(int B);
 bool heads_tc_supported(int B, int H, const void* h, const void* w1, const void* w2);
 medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t* w2, int B, int H, int V, int K,
-                           uint16_t* u2, float* z, int32_t* d_status, cudaStream_t s);
+                           uint16_t* u2, float* z, float* gmax, int32_t* d_status, cudaStream_t s);
+inline int heads_tc_groups(int V) { return 4 * ceil_div(V, 128); }
 
-// Scratch of the tensor-core path: u split into hi/lo bf16 rows, z, top-k candidates.
-static size_t heads_tc_ws_bytes(int B, int H, int V, int K, int topk) {
+// Scratch of the tensor-core path: u split into hi/lo bf16 rows, z, the
+// maxima of z's 32-row groups.
+static size_t heads_tc_ws_bytes(int B, int H, int V, int K) {
   WsCarver w(nullptr);
   w.take<uint16_t>((size_t)K * 2 * heads_tc_bp(B) * H);
   w.take<float>((size_t)B * K * V);
-  w.take<float>((size_t)B * K * chunks_for(V) * topk);
-  w.take<int>((size_t)B * K * chunks_for(V) * topk);
+  w.take<float>((size_t)B * K * heads_tc_groups(V));
   return w.used;
 }
 
 static size_t heads_ws_bytes(int B, int H, int V, int K, int topk) {
   if (B >= 4 && B <= 64 && H % 64 == 0) {
     // either path may run (the tensor-core one for bf16): size for both
-    const size_t a = heads_tc_ws_bytes(B, H, V, K, topk);
+    const size_t a = heads_tc_ws_bytes(B, H, V, K);
     WsCarver w(nullptr);
     w.take<float>((size_t)B * K * H);
     w.take<float>(heads_cand(B, V, K, topk));
@@ -727,13 +848,15 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
     WsCarver wt(ws);
     uint16_t* u2 = wt.take<uint16_t>((size_t)K * 2 * heads_tc_bp(B) * H);
     float* zt = wt.take<float>((size_t)B * K * V);
-    float* cvt = wt.take<float>((size_t)B * K * chunks_for(V) * topk);
-    int* cit = wt.take<int>((size_t)B * K * chunks_for(V) * topk);
+    float* gm = wt.take<float>((size_t)B * K * heads_tc_groups(V));
     float* z = logits_or_null ? logits_or_null : zt;
     medusa_status st = heads_tc_run((const uint16_t*)h, (const uint16_t*)w1, (const uint16_t*)w2, B, H, V, K, u2, z,
-                                    d_status, s);
+                                    gm, d_status, s);
     if (st != MEDUSA_OK) return st;
-    return launch_topk(z, nullptr, B * K, V, topk, cvt, cit, topk_logit, topk_idx, s);
+    // one ranking kernel, reading only the groups that can hold a top-k logit
+    launch_pdl(topk_groups_kernel, dim3(B * K), dim3(kRowThreads), 0, s, (const float*)z, (const float*)gm, V,
+               heads_tc_groups(V), topk, topk_logit, topk_idx);
+    return launch_status();
   }
   WsCarver wc(ws);
   float* u = wc.take<float>((size_t)B * K * H);

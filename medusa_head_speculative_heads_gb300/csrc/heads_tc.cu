@@ -11,8 +11,10 @@
 // sums D[:, b] + D[:, Bp + b] and the product keeps the fp32 vector's
 // precision.  For W1, X = h (exact in bf16: no lo part, so the product has Bp
 // columns); the W1 epilogue applies SiLU and the residual and writes u
-// split into hi/lo for W2.  The W2 epilogue writes the fp32 logits z, which
-// the regular top-k kernels then rank.
+// split into hi/lo for W2.  The W2 epilogue writes the fp32 logits z and, for
+// every batch row, the maximum of each 32-row group (one warp's rows, by a
+// shuffle transpose-reduction), which the group ranking kernel uses to read
+// only the few groups that can hold a top-k logit.
 //
 // Roles (256 threads, one CTA per SM, persistent over 128-row tiles): warp 0
 // lane 0 issues TMA loads of the A (weights) and B (vector) tiles into a ring
@@ -63,6 +65,7 @@ struct Params {
   const uint16_t* h;      // [B][H] bf16 (W1 residual)
   uint16_t* u2;           // [K][N][H] bf16, W1 output (hi rows, then lo rows)
   float* z;               // [B][K][R] fp32, W2 output
+  float* gmax;            // [B][K][4 tiles_per_head] fp32, W2: maximum of each 32-row group of z
   int32_t* d_status;
 };
 
@@ -73,6 +76,38 @@ struct Bars {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const bool ok = mbar_wait_bounded(bar, parity, abort, kWaitNs);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Column maxima of a warp: on entry a[0..N) holds this lane's values of N
+// columns (N a power of two, 16 to 64).  Each step with lane offset O halves
+// the columns a lane keeps (the lane with bit O set keeps the upper half) and
+// takes the maximum with the partner's copy of them; once a lane keeps one
+// column the remaining steps only combine partners.  On return lane L holds
+// the warp maximum of columns 2L and 2L + 1 in a[0], a[1] (N = 64), of column
+// L (N = 32), or of column L / 2 (N = 16).
+template <int CUR, int O, int N>
+__device__ __forceinline__ void warp_colmax_step(float (&a)[N], int lane) {
+  if constexpr (O > 0) {
+    if constexpr (CUR > 1) {
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < CUR / 2; ++i) {
+        const float send = up ? a[i] : a[i + CUR / 2];
+        const float keep = up ? a[i + CUR / 2] : a[i];
+        a[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+      }
+      warp_colmax_step<CUR / 2, O / 2, N>(a, lane);
+    } else {
+      a[0] = fmaxf(a[0], __shfl_xor_sync(0xffffffffu, a[0], O));
+      warp_colmax_step<1, O / 2, N>(a, lane);
+    }
+  }
+}
+
+template <int N, int O>
+__device__ __forceinline__ void warp_colmax(float (&a)[N], int lane) {
+  static_assert(N == 16 || N == 32 || N == 64, "columns");
+  warp_colmax_step<N, O, N>(a, lane);
 }
 
 }  // namespace htc
@@ -224,19 +259,46 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[ab]);
       const int k = tile / p.tiles_per_head, row = (tile % p.tiles_per_head) * 128 + m;
-      if (row >= p.R) continue;
+      if (p.first) {
+        if (row >= p.R) continue;
 #pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        const float zsum = p.first ? v[b] : v[b] + v[BP + b];
-        if (p.first) {
+        for (int b = 0; b < BP; ++b) {
           float val = 0.f;
-          if (b < p.B) val = zsum / (1.f + expf(-zsum)) + bf16_bits_to_f32((hres[b >> 1] >> (16 * (b & 1))) & 0xffffu);
+          if (b < p.B) val = v[b] / (1.f + expf(-v[b])) + bf16_bits_to_f32((hres[b >> 1] >> (16 * (b & 1))) & 0xffffu);
           const uint32_t hi = f32_to_bf16_bits(val);
           const uint32_t lo = f32_to_bf16_bits(val - bf16_bits_to_f32(hi));
           p.u2[((size_t)k * p.N + b) * p.H + row] = (uint16_t)hi;
           p.u2[((size_t)k * p.N + BP + b) * p.H + row] = (uint16_t)lo;
-        } else if (b < p.B) {
-          p.z[((size_t)b * p.K + k) * p.R + row] = zsum;
+        }
+      } else {
+        // z = hi and lo products summed; rows past the vocabulary and padded
+        // batch columns enter the group maxima as -inf.
+        constexpr int RB = BP > 32 ? 64 : BP;  // columns of the warp reduction (a power of two)
+        float a[RB];
+#pragma unroll
+        for (int b = 0; b < BP; ++b) a[b] = (b < p.B && row < p.R) ? v[b] + v[BP + b] : -INFINITY;
+#pragma unroll
+        for (int b = BP; b < RB; ++b) a[b] = -INFINITY;
+        if (row < p.R) {
+#pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < p.B) p.z[((size_t)b * p.K + k) * p.R + row] = a[b];
+        }
+        // Maximum of this warp's 32 rows for every batch column, for the
+        // ranking kernel: it skips every 32-row group whose maximum is below
+        // its threshold.
+        warp_colmax<RB, 16>(a, lane);
+        const int groups = 4 * p.tiles_per_head, gi = (tile % p.tiles_per_head) * 4 + (warp - 4);
+        if constexpr (RB == 64) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int b = 2 * lane + i;
+            if (b < p.B) p.gmax[((size_t)b * p.K + k) * groups + gi] = a[i];
+          }
+        } else if constexpr (RB == 32) {
+          if (lane < p.B) p.gmax[((size_t)lane * p.K + k) * groups + gi] = a[0];
+        } else {
+          if (!(lane & 1) && (lane >> 1) < p.B) p.gmax[((size_t)(lane >> 1) * p.K + k) * groups + gi] = a[0];
         }
       }
     }
@@ -288,9 +350,10 @@ bool heads_tc_supported(int B, int H, const void* h, const void* w1, const void*
 }
 
 // Both passes: u2 = split(SiLU(W1 h) + h) ([K][2Bp][H] bf16, caller scratch),
-// then z = W2 u ([B][K][V] fp32).
+// then z = W2 u ([B][K][V] fp32) and the maximum of every 32-row group of z
+// ([B][K][4 ceil(V / 128)] fp32, groups past V hold -inf).
 medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t* w2, int B, int H, int V, int K,
-                           uint16_t* u2, float* z, int32_t* d_status, cudaStream_t s) {
+                           uint16_t* u2, float* z, float* gmax, int32_t* d_status, cudaStream_t s) {
   const int Bp = heads_tc_bp(B), N = 2 * Bp;
   CUtensorMap ma1, mb1, ma2, mb2;
   if (!map_rows(&ma1, w1, H, (long long)K * H, 128) || !map_rows(&mb1, h, H, B, Bp) ||
@@ -319,6 +382,7 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   p.h = h;
   p.u2 = u2;
   p.z = z;
+  p.gmax = gmax;
   p.d_status = d_status;
   // W1: rows per head = H
   p.R = H;

@@ -66,6 +66,11 @@ def test_heads_parity(mg, case):
     checked, flagged = check_topk(to_host(idx), to_host(val), ref["z"], _tau(c["dtype"]), TOL[c["dtype"]])
     assert flagged <= max(1, checked // 50)
     assert mg.medusa_status_check(st) == 0
+    # the ranking itself is exact: the top-k of the logits the kernel wrote
+    zg = to_host(z).reshape(-1, c["V"])
+    own_idx, own_val = oracle.topk_f32(zg, c["topk"])
+    np.testing.assert_array_equal(to_host(idx).reshape(own_idx.shape), own_idx)
+    np.testing.assert_array_equal(to_host(val).reshape(own_idx.shape).astype(np.float64), own_val)
     # without the optional logits output (workspace path) the result is identical
     idx2, val2 = mg.medusa_heads(to_dev(h), to_dev(w1), to_dev(w2), c["topk"])
     torch.cuda.synchronize()
@@ -119,6 +124,30 @@ def test_head_topk_when_the_best_values_crowd_a_few_threads(mg):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(to_host(idx), ref_idx)
         np.testing.assert_array_equal(to_host(val).astype(np.float64), ref_val)
+
+
+@pytest.mark.parametrize("distinct", [2, 8])
+def test_heads_batch_ranking_exact_ties(mg, distinct):
+    """Tensor-core heads (B = 8) on inputs whose logits are exact in fp32 in any
+    summation order: W1 = 0 (so u = SiLU(0) + h = h), h in multiples of 1/8,
+    W2 rows with entries in {-1, 0, 1}, only `distinct` different rows tiled
+    over the vocabulary.  Every logit value repeats V / distinct times: with
+    two distinct rows more candidates reach the ranking threshold than its
+    shared-memory list holds (the whole-row rounds run), with eight they fit.
+    Bit-exact against the oracle, ties ranked by index."""
+    B, H, V, K, topk = 8, 1024, 8000, 2, 10
+    g = np.random.default_rng(11 + distinct)
+    h = wl.to_bf16_bits((np.clip(np.round(g.standard_normal((B, H)) * 8), -32, 32) / 8).astype(np.float32))
+    w1 = np.zeros((K, H, H), np.uint16)
+    base = g.integers(-1, 2, size=(K, distinct, H)).astype(np.float32)
+    w2 = wl.to_bf16_bits(base[:, np.arange(V) % distinct, :])
+    ref = oracle.heads(h, w1, w2, topk)
+    st = _status(mg)
+    idx, val = mg.medusa_heads(to_dev(h), to_dev(w1), to_dev(w2), topk, d_status=st)
+    torch.cuda.synchronize()
+    assert mg.medusa_status_check(st) == 0
+    np.testing.assert_array_equal(to_host(idx), ref["idx"])
+    np.testing.assert_array_equal(to_host(val).astype(np.float64), ref["val"])
 
 
 # ----------------------------------------------------------------------------- tree build
