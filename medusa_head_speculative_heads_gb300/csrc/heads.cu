@@ -439,6 +439,25 @@ __device__ __forceinline__ void block_best(float& v, int& id, float* sv, int* si
   __syncthreads();
 }
 
+// Bitonic sort of one (value, index) pair per lane across the warp, best
+// first (value descending, index ascending): afterwards lane r holds the
+// pair of rank r.  Every lane must take part.
+__device__ __forceinline__ void warp_sort32(float& v, int& id) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+      const int oi = __shfl_xor_sync(0xffffffffu, id, j);
+      // in a block of k lanes sorted best-first (bit k clear) the lower lane
+      // of each pair keeps the better element; in the others, the worse
+      const bool keep_better = ((lane & j) == 0) == ((lane & k) == 0);
+      if (keep_better == ranks_ahead(ov, oi, v, id)) { v = ov; id = oi; }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRowThreads)
 topk_rows_kernel(const float* __restrict__ x, int n, int topk, float* __restrict__ out_v, int* __restrict__ out_i) {
   __shared__ float cv[kRowCap];
@@ -558,15 +577,17 @@ constexpr int kRowTopkMax = 32;  // topk the row kernels rank
 
 // Top-k of rows whose 32-element group maxima are known (written by the
 // tensor-core W2 epilogue): one CTA per row.
-//  1. Every thread takes the best (maximum, group) of its groups; the topk-th
-//     best of these thread bests (warp 0), value T, is at most the row's
-//     topk-th best value (topk distinct groups, hence topk distinct elements,
-//     reach T).
+//  1. Every thread takes the best (maximum, group) of its groups (loads four
+//     at a time in flight); lane L of warp 0 takes the best of threads
+//     L, L + 32, ..., so the 32 lane bests come from disjoint sets of groups.
+//     Their topk-th best value T (a warp sort) is at most the row's topk-th
+//     best value (topk distinct groups, hence topk distinct elements, reach T).
 //  2. Only the groups whose maximum reaches T can hold a value >= T; their
 //     elements >= T (every top-k element among them) go to shared memory.
-//  3. topk rounds of a warp argmax over those candidates, as in
+//  3. Up to 32 candidates (about topk + a few for smooth logits) are ranked
+//     by one warp sort; more, by topk rounds of a warp argmax as in
 //     topk_rows_kernel, with the same whole-row fallback when they overflow.
-// Grid rows; gmax[row][groups], group g = elements [32 g, 32 g + 32).
+// topk <= 32.  Grid rows; gmax[row][groups], group g = elements [32 g, 32 g + 32).
 __global__ void __launch_bounds__(kRowThreads)
 topk_groups_kernel(const float* __restrict__ x, const float* __restrict__ gmax, int n, int groups, int topk,
                    float* __restrict__ out_v, int* __restrict__ out_i) {
@@ -577,68 +598,96 @@ topk_groups_kernel(const float* __restrict__ x, const float* __restrict__ gmax, 
   __shared__ int s_count;
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.x, tid = threadIdx.x;
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const float* xr = x + (size_t)row * n;
   const float* gr = gmax + (size_t)row * groups;
-  // 1. thread bests over the group maxima, then the topk-th best of them
+  constexpr int GU = 4;  // group maxima a thread has in flight
+  // 1. thread bests over the group maxima
   float mv = -INFINITY;
   int mg = INT_MAX;
-  for (int g = tid; g < groups; g += kRowThreads) {
-    const float v = gr[g];
-    if (ranks_ahead(v, g, mv, mg)) { mv = v; mg = g; }
+  for (int g0 = tid; g0 < groups; g0 += kRowThreads * GU) {
+    float t[GU];
+#pragma unroll
+    for (int u = 0; u < GU; ++u) {
+      const int g = g0 + u * kRowThreads;
+      t[u] = g < groups ? gr[g] : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < GU; ++u) {
+      const int g = g0 + u * kRowThreads;
+      if (g < groups && ranks_ahead(t[u], g, mv, mg)) { mv = t[u]; mg = g; }
+    }
   }
   cv[tid] = mv;
   ci[tid] = mg;
   __syncthreads();
   if (tid < 32) {
-    float pv = INFINITY;
-    int pi = -1;
-    for (int r = 0; r < topk; ++r) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
+    // lane best over threads lane, lane + 32, ...; then topk rounds of a warp
+    // argmax over the 32 lane bests, the winner dropping out each round
+    float lv = cv[lane];
+    int lg = ci[lane];
 #pragma unroll
-      for (int j = tid; j < kRowThreads; j += 32)
-        if (ranks_ahead(pv, pi, cv[j], ci[j]) && ranks_ahead(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
-      warp_best(bv, bi);
-      pv = bv;
-      pi = bi;
-    }
-    if (tid == 0) { sv[0] = pv; s_count = 0; }
+    for (int w = 1; w < kRowThreads / 32; ++w)
+      if (ranks_ahead(cv[lane + 32 * w], ci[lane + 32 * w], lv, lg)) { lv = cv[lane + 32 * w]; lg = ci[lane + 32 * w]; }
+    warp_sort32(lv, lg);
+    const float T = __shfl_sync(0xffffffffu, lv, topk - 1);
+    if (lane == 0) { sv[0] = T; s_count = 0; }
   }
   __syncthreads();
   const float T = sv[0];
   // 2. elements >= T of the groups that reach T
   const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15u) == 0;
-  for (int g = tid; g < groups; g += kRowThreads) {
-    if (!(gr[g] >= T)) continue;
-    const int e0 = 32 * g;
-    if (vec && e0 + 32 <= n) {
-      float4 t[8];
+  auto take = [&](float v, int i) {
+    if (v >= T) {
+      const int slot = atomicAdd(&s_count, 1);
+      if (slot < kRowCap) { cv[slot] = v; ci[slot] = i; }
+    }
+  };
+  for (int g0 = tid; g0 < groups; g0 += kRowThreads * GU) {
+    float t[GU];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) t[q] = reinterpret_cast<const float4*>(xr + e0)[q];
+    for (int u = 0; u < GU; ++u) {
+      const int g = g0 + u * kRowThreads;
+      t[u] = g < groups ? gr[g] : -INFINITY;
+    }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float e[4] = {t[q].x, t[q].y, t[q].z, t[q].w};
+    for (int u = 0; u < GU; ++u) {
+      const int g = g0 + u * kRowThreads;
+      if (g >= groups || !(t[u] >= T)) continue;
+      const int e0 = 32 * g;
+      if (vec && e0 + 32 <= n) {
+        float4 q4[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (e[c] >= T) {
-            const int slot = atomicAdd(&s_count, 1);
-            if (slot < kRowCap) { cv[slot] = e[c]; ci[slot] = e0 + 4 * q + c; }
-          }
-      }
-    } else {
-      for (int i = e0; i < e0 + 32 && i < n; ++i) {
-        const float v = xr[i];
-        if (v >= T) {
-          const int slot = atomicAdd(&s_count, 1);
-          if (slot < kRowCap) { cv[slot] = v; ci[slot] = i; }
+        for (int q = 0; q < 8; ++q) q4[q] = reinterpret_cast<const float4*>(xr + e0)[q];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          take(q4[q].x, e0 + 4 * q);
+          take(q4[q].y, e0 + 4 * q + 1);
+          take(q4[q].z, e0 + 4 * q + 2);
+          take(q4[q].w, e0 + 4 * q + 3);
         }
+      } else {
+        for (int i = e0; i < e0 + 32 && i < n; ++i) take(xr[i], i);
       }
     }
   }
   __syncthreads();
   const int c = s_count;
-  // 3. topk rounds, each the best candidate ranked behind the previous winner
+  // 3. at most 32 candidates (the usual case): one warp sort, ranks 0 .. topk-1
+  // in lanes 0 .. topk-1; more: topk rounds, each the best candidate ranked
+  // behind the previous winner
+  if (c <= 32) {
+    if (tid < 32) {
+      float v = tid < c ? cv[tid] : -INFINITY;
+      int id = tid < c ? ci[tid] : INT_MAX;
+      warp_sort32(v, id);
+      if (tid < topk) {
+        out_v[(size_t)row * topk + tid] = v;
+        out_i[(size_t)row * topk + tid] = id;
+      }
+    }
+    return;
+  }
   float pv = INFINITY;
   int pi = -1;
   if (c <= kRowCap) {

@@ -18,7 +18,7 @@
 //
 // Roles (256 threads, one CTA per SM, persistent over 128-row tiles): warp 0
 // lane 0 issues TMA loads of the A (weights) and B (vector) tiles into a ring
-// of 6 to 10 stages (the smaller the batch, the smaller the B tile and the
+// of 7 to 11 stages (the smaller the batch, the smaller the B tile and the
 // more weight bytes in flight); warp 1 allocates TMEM and lane 0 issues the
 // MMAs (four K=16 steps per 64-column stage) into one of two accumulators;
 // warps 4-7 read the accumulator (one row per thread) and write the outputs,
@@ -39,7 +39,7 @@ using namespace sm100;
 namespace htc {
 
 constexpr int kThreads = 256;
-constexpr int kMaxStages = 10;
+constexpr int kMaxStages = 12;
 constexpr uint32_t kATile = 16384;  // 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
 
@@ -47,13 +47,14 @@ constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
 template <int BP>
 struct Ring {
   static constexpr uint32_t kStageBytes = kATile + 256u * BP;
-  static constexpr int kStages = (int)(200u * 1024u / kStageBytes) < kMaxStages ? (int)(200u * 1024u / kStageBytes)
+  static constexpr int kStages = (int)(224u * 1024u / kStageBytes) < kMaxStages ? (int)(224u * 1024u / kStageBytes)
                                                                                  : kMaxStages;
   static constexpr uint32_t kOffBar = kStages * kStageBytes;
   static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
   static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
+constexpr int kNextBoxes = 24;  // W2 boxes per CTA the W1 pass brings into L2
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -62,6 +63,7 @@ struct Params {
   int mma_n;              // columns of the product: N (W2: hi and lo rows), Bp (W1: h is exact in bf16)
   int tiles_per_head, tiles;
   int first;              // 1: W1 pass, 0: W2 pass
+  int next_R, next_tiles_per_head, next_tiles;  // W1 pass: the W2 pass's geometry (its first boxes go to L2)
   const uint16_t* h;      // [B][H] bf16 (W1 residual)
   uint16_t* u2;           // [K][N][H] bf16, W1 output (hi rows, then lo rows)
   float* z;               // [B][K][R] fp32, W2 output
@@ -115,7 +117,7 @@ __device__ __forceinline__ void warp_colmax(float (&a)[N], int lane) {
 template <int BP>
 __global__ void __launch_bounds__(htc::kThreads, 1)
 heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                const htc::Params p) {
+                const __grid_constant__ CUtensorMap tm_next, const htc::Params p) {
   constexpr int NC = 2 * BP;  // accumulator columns
   using namespace htc;
   constexpr int kStages = Ring<BP>::kStages;
@@ -144,17 +146,37 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
+  const int ksteps = p.H / 64;
+  // Each CTA walks the K blocks of its tiles starting at its own offset, so
+  // CTAs working in step do not all read the same vector box from L2 at once.
+  const int k_rot = (int)((blockIdx.x * 5u) % (unsigned)ksteps);
   if (warp == 0 && lane == 0) {
     tma_prefetch(&tm_a);
     tma_prefetch(&tm_b);
-    // While an earlier kernel on the stream finishes, bring the weight boxes
-    // of this CTA's first ring fill into L2 (a hint with no data dependence:
-    // the loads after the dependency wait read whatever is current).
+    // The weights are never written during a call, so before the dependency
+    // wait: bring this CTA's first ring fill into L2 (in the order the loads
+    // will want it) while an earlier kernel finishes, and in the W1 pass also
+    // the next kStages .. kStages + kNextBoxes boxes of the first tile that
+    // the W2 CTA of the same index will stream (its first kStages it fetches
+    // itself).  The W1 weight loads are marked evict-first, so these lines
+    // stay in L2 while the W1 pass streams through it.
+    const int n = kStages < ksteps ? kStages : ksteps;
     if ((int)blockIdx.x < p.tiles) {
       const int tile = blockIdx.x;
       const int k = tile / p.tiles_per_head, m0 = (tile % p.tiles_per_head) * 128;
-      const int n = kStages < p.H / 64 ? kStages : p.H / 64;
-      for (int kk = 0; kk < n; ++kk) tma_prefetch_l2_2d(&tm_a, kk * 64, k * p.R + m0);
+      for (int i = 0; i < n; ++i) {
+        const int kk = i + k_rot < ksteps ? i + k_rot : i + k_rot - ksteps;
+        tma_prefetch_l2_2d(&tm_a, kk * 64, k * p.R + m0);
+      }
+    }
+    if (p.first && (int)blockIdx.x < p.next_tiles) {
+      const int tile = blockIdx.x;
+      const int k = tile / p.next_tiles_per_head, m0 = (tile % p.next_tiles_per_head) * 128;
+      const int hi = n + kNextBoxes < ksteps ? n + kNextBoxes : ksteps;
+      for (int i = n; i < hi; ++i) {
+        const int kk = i + k_rot < ksteps ? i + k_rot : i + k_rot - ksteps;
+        tma_prefetch_l2_2d(&tm_next, kk * 64, k * p.next_R + m0);
+      }
     }
   }
   tc_fence_before();
@@ -163,17 +185,14 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   pdl_wait();
   pdl_trigger();
   const uint32_t tmem = s_tmem;
-  const int ksteps = p.H / 64;
   const uint32_t b_bytes = (uint32_t)p.mma_n * 128;
-  // Each CTA walks the K blocks of its tiles starting at its own offset, so
-  // CTAs working in step do not all read the same vector box from L2 at once.
-  const int k_rot = (int)((blockIdx.x * 5u) % (unsigned)ksteps);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int g = 0;
       bool alive = true;
+      const uint64_t once = l2_policy_evict_first();  // every weight byte is read once per call
       for (int tile = blockIdx.x; tile < p.tiles && alive; tile += gridDim.x) {
         const int k = tile / p.tiles_per_head, m0 = (tile % p.tiles_per_head) * 128;
         for (int i = 0; i < ksteps; ++i, ++g) {
@@ -184,7 +203,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
             break;
           uint8_t* st = smem + s * kStageBytes;
           mbar_expect_tx(&bars->full[s], kATile + b_bytes);
-          tma_load_2d(st, &tm_a, &bars->full[s], kk * 64, k * p.R + m0);
+          tma_load_2d_hint(st, &tm_a, &bars->full[s], kk * 64, k * p.R + m0, once);
           tma_load_2d(st + kATile, &tm_b, &bars->full[s], kk * 64, p.first ? 0 : k * p.N);
         }
       }
@@ -390,14 +409,17 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   p.mma_n = Bp;
   p.tiles_per_head = ceil_div(H, 128);
   p.tiles = K * p.tiles_per_head;
-  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma1, mb1, p);
+  p.next_R = V;
+  p.next_tiles_per_head = ceil_div(V, 128);
+  p.next_tiles = grid_for(K * p.next_tiles_per_head);  // the W2 CTAs' first tiles
+  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma1, mb1, ma2, p);
   // W2: rows per head = V
   p.R = V;
   p.first = 0;
   p.mma_n = N;
   p.tiles_per_head = ceil_div(V, 128);
   p.tiles = K * p.tiles_per_head;
-  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma2, mb2, p);
+  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma2, mb2, ma2, p);
   return launch_status();
 }
 
