@@ -529,6 +529,26 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       else { r = x.mt * 128 + m; h = x.h0; }
       const int node = r / p.G, gq = r % p.G;
       const bool row_ok = node < p.N && h < p.Hkv;
+      // The ancestor-mask words of this thread's keys in the tree key tiles
+      // (one tile for two-head tiles: N <= 64 keys of 64; two otherwise:
+      // N <= 256 keys of 128), loaded when the unit starts.  Loaded at the
+      // tree tile itself, they waited an L2 round trip under the cache stream
+      // (a tree tile's mask step measured ~5700 cycles against ~100 for a
+      // prefix tile).  Keys at or past N are cleared here.
+      constexpr int kTT = PACKED ? 1 : 2;
+      constexpr int MW = NC / 32;
+      uint32_t tmw[kTT][MW];
+#pragma unroll
+      for (int tt = 0; tt < kTT; ++tt) {
+#pragma unroll
+        for (int wv = 0; wv < MW; ++wv) {
+          const int j = tt * p.KT + koff + 32 * wv;  // first key of the word (a multiple of 32)
+          uint32_t mk = (row_ok && j < p.N) ? __ldg(p.mask + (size_t)node * p.W + (j >> 5)) : 0u;
+          const int lim = p.N - j;
+          if (lim < 32) mk &= lim <= 0 ? 0u : ((1u << lim) - 1u);
+          tmw[tt][wv] = mk;
+        }
+      }
       float m_used = -INFINITY, l = 0.f;
       for (int t = w.t0; t < w.t1; ++t, ++g) {
         const int sb = g & 1;
@@ -551,18 +571,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           // keys entirely inside the prefix: every one is visible
 #pragma unroll
           for (int c = 0; c < NC; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
-        } else {
-          uint32_t mw[NC / 32];
+        } else if (tree) {
+          // ancestors only (the words above; tree tile t - n_pre < kTT)
+          const bool second = kTT > 1 && t - x.n_pre > 0;
+          uint32_t mw[MW];
 #pragma unroll
-          for (int w = 0; w < NC / 32; ++w) {
-            const int word = (j0 >> 5) + w;
-            mw[w] = (tree && row_ok && word < p.W) ? p.mask[(size_t)node * p.W + word] : 0u;
-          }
+          for (int wv = 0; wv < MW; ++wv) mw[wv] = second ? tmw[kTT - 1][wv] : tmw[0][wv];
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
-            const int j = j0 + c;
-            const bool v = row_ok && (tree ? (j < p.N && ((mw[c >> 5] >> (c & 31)) & 1u)) : (j < x.L));
-            s[c] = v ? s[c] : -INFINITY;
+            s[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+            m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+          }
+        } else {
+          // the last prefix tile, partly past prefix_len (or a row that does not exist)
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            s[c] = (row_ok && j0 + c < x.L) ? s[c] : -INFINITY;
             m4[c & 3] = fmaxf(m4[c & 3], s[c]);
           }
         }
