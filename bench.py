@@ -319,7 +319,7 @@ def run_profile(args, c, mg, topo, dev):
     if args.profile not in ("linear", "head_loss") and vs.check() != 0:
         raise RuntimeError("device status set")
     us = a.elapsed_time(b) / args.steps * 1e3
-    line = {"profile": args.profile, "workload": f"{c['name']} B={c['B']} nodes={N}", "calls": args.steps,
+    line = {"profile": args.profile, "workload": f"{c['name']} B={c['B']} nodes={N} layers={c['nl']} heads={c['Hq']}/{c['Hkv']} prefix={c['L']}", "calls": args.steps,
             "us_per_call": round(us, 2)}
     if args.profile in ("heads", "attention"):
         hbm, tflops, _ = _peaks()
