@@ -7,11 +7,14 @@
 // gathered from the tree K/V buffers to rows prefix_len .. prefix_len +
 // accept_len - 1 of every layer.
 //
-// Kernel 1 moves 16-byte (or 4-byte) words: one thread per word of every
-// (layer, row, path slot, kv head) row; slots past accept_len do nothing.
+// Kernel 1 moves 16-byte (or 4-byte) words: one CTA per (layer, row, path
+// slot, K or V) row of Hkv x d elements at a time (decode and checks once per
+// CTA, two words in flight per thread); slots past accept_len do nothing.
 // Kernel 2 writes new_len after kernel 1 has read prefix_len, so new_len may
 // alias prefix_len; when it does not, kernel 1's first B threads write it
 // and kernel 2 is not launched.
+#include <limits.h>
+
 #include "common.cuh"
 #include "host_util.h"
 
@@ -35,24 +38,26 @@ __global__ void kv_gather_kernel(WORD* __restrict__ kc, WORD* __restrict__ vc, c
                                  const WORD* __restrict__ vt, const int32_t* __restrict__ path_nodes,
                                  const int32_t* __restrict__ accept_len, const int32_t* __restrict__ prefix_len,
                                  int nl, int B, int N, int Lmax, int Dmax, int words_per_row,
-                                 long long total, int32_t* d_status, int32_t* __restrict__ new_len_separate) {
+                                 int rows_total, int32_t* d_status, int32_t* __restrict__ new_len_separate) {
   pdl_wait();
   pdl_trigger();
   if (new_len_separate) {  // does not alias prefix_len: written here, no second kernel
     const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     if (b < B) new_len_separate[b] = kv_new_len(prefix_len, accept_len, path_nodes, (int)b, Lmax, Dmax, N);
   }
-  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-       t += (long long)gridDim.x * blockDim.x) {
-    // t = (((l * B + b) * (Dmax+1) + i) * words_per_row + w) * 2 + kv
-    long long r = t;
-    const int kv = (int)(r & 1); r >>= 1;
-    const int w = (int)(r % words_per_row); r /= words_per_row;
-    const int i = (int)(r % (Dmax + 1)); r /= (Dmax + 1);
-    const int b = (int)(r % B);
-    const int l = (int)(r / B);
+  // One CTA per (layer, row, path slot, K or V) row of words at a time: the
+  // decode, the checks and the source slot are per CTA, the threads move
+  // the row's words.  row = ((l * B + b) * (Dmax + 1) + i) * 2 + kv.
+  for (int row = blockIdx.x; row < rows_total; row += gridDim.x) {
+    int r = row;
+    const int kv = r & 1;
+    r >>= 1;
+    const int i = r % (Dmax + 1);
+    r /= Dmax + 1;
+    const int b = r % B;
+    const int l = r / B;
     const int A = accept_len[b], L = prefix_len[b];
-    const bool first = (l == 0 && i == 0 && w == 0 && kv == 0);
+    const bool first = l == 0 && i == 0 && kv == 0 && threadIdx.x == 0;
     if (A < 1 || A > Dmax + 1 || L < 0) {
       if (first) set_status(d_status, MEDUSA_DEV_BAD_INDEX);
       continue;
@@ -73,10 +78,15 @@ __global__ void kv_gather_kernel(WORD* __restrict__ kc, WORD* __restrict__ vc, c
       continue;
     }
     const int src = path_nodes[(size_t)b * (Dmax + 1) + i];
-    const size_t so = (((size_t)l * B + b) * N + src) * words_per_row + w;
-    const size_t dof = (((size_t)l * B + b) * Lmax + L + i) * words_per_row + w;
-    if (kv == 0) kc[dof] = kt[so];
-    else vc[dof] = vt[so];
+    const WORD* from = (kv ? vt : kt) + (((size_t)l * B + b) * N + src) * words_per_row;
+    WORD* to = (kv ? vc : kc) + (((size_t)l * B + b) * Lmax + L + i) * words_per_row;
+    int w = threadIdx.x;
+    for (; w + blockDim.x < words_per_row; w += 2 * blockDim.x) {  // two words in flight per thread
+      const WORD a = from[w], c = from[w + blockDim.x];
+      to[w] = a;
+      to[w + blockDim.x] = c;
+    }
+    if (w < words_per_row) to[w] = from[w];
   }
 }
 
@@ -116,11 +126,14 @@ extern "C" medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, c
   if (!v16 && (row_bytes % 4 || ((uintptr_t)kc | (uintptr_t)vc | (uintptr_t)kt | (uintptr_t)vt) & 3u))
     return MEDUSA_ERR_INVALID_ARG;
   const int wpr = (int)(row_bytes / (v16 ? 16 : 4));
-  const long long total = (long long)n_layers * B * (Dmax + 1) * wpr * 2;
-  const int threads = 256;
-  long long blocks = (total + threads - 1) / threads;
+  const long long rows_ll = (long long)n_layers * B * (Dmax + 1) * 2;
+  if (rows_ll > INT_MAX) return MEDUSA_ERR_INVALID_ARG;
+  const int rows_total = (int)rows_ll;
+  const int threads = wpr >= 256 ? 256 : (wpr + 31) / 32 * 32;
+  long long blocks = rows_total;
   const long long cap = (long long)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
+  if (blocks * threads < B) blocks = (B + threads - 1) / threads;  // the first B threads write new_len
   // One kernel when new_len is a separate buffer the grid's first B threads can write.
   const bool fused = !overlaps(new_len, (size_t)B * 4, prefix_len, (size_t)B * 4) && blocks * threads >= B;
   int32_t* nl_sep = fused ? new_len : nullptr;
@@ -128,12 +141,12 @@ extern "C" medusa_status medusa_kv_compact(void* kc, void* vc, const void* kt, c
     launch_pdl(kv_gather_kernel<uint4>, dim3((int)blocks), dim3(threads), 0, s, (uint4*)kc, (uint4*)vc, (const uint4*)kt,
                                                            (const uint4*)vt, path_nodes, accept_len,
                                                            prefix_len, n_layers, B, N, Lmax, Dmax,
-                                                           wpr, total, d_status, nl_sep);
+                                                           wpr, rows_total, d_status, nl_sep);
   else
     launch_pdl(kv_gather_kernel<uint32_t>, dim3((int)blocks), dim3(threads), 0, s, (uint32_t*)kc, (uint32_t*)vc,
                                                                (const uint32_t*)kt, (const uint32_t*)vt,
                                                                path_nodes, accept_len, prefix_len,
-                                                               n_layers, B, N, Lmax, Dmax, wpr, total,
+                                                               n_layers, B, N, Lmax, Dmax, wpr, rows_total,
                                                                d_status, nl_sep);
   if (!fused)
     launch_pdl(kv_len_kernel, dim3((B + 127) / 128), dim3(128), 0, s, prefix_len, accept_len, new_len, B, Lmax,
