@@ -576,150 +576,168 @@ topk_rows_kernel(const float* __restrict__ x, int n, int topk, float* __restrict
 constexpr int kRowTopkMax = 32;  // topk the row kernels rank
 
 // Top-k of rows whose 32-element group maxima are known (written by the
-// tensor-core W2 epilogue): one CTA per row.
-//  1. Every thread takes the best (maximum, group) of its groups (loads four
-//     at a time in flight); lane L of warp 0 takes the best of threads
-//     L, L + 32, ..., so the 32 lane bests come from disjoint sets of groups.
-//     Their topk-th best value T (a warp sort) is at most the row's topk-th
-//     best value (topk distinct groups, hence topk distinct elements, reach T).
-//  2. Only the groups whose maximum reaches T can hold a value >= T; their
-//     elements >= T (every top-k element among them) go to shared memory.
+// tensor-core W2 epilogue): one warp per row, no block barrier.
+//  1. Each lane loads the maxima of its groups (16-byte loads, all in flight
+//     for up to kGroupRegs x 4 groups per lane) and takes their best (value,
+//     group).  The lanes' group sets are disjoint, so the topk-th best of the
+//     32 lane bests (a warp bitonic sort), T, is at most the row's topk-th
+//     best value: topk distinct groups, hence topk distinct elements, reach it.
+//  2. Only groups whose maximum reaches T can hold a value >= T; each lane
+//     reads its own such groups (eight 16-byte loads each, usually none or
+//     one per lane) and appends their values >= T (every top-k element among
+//     them) to the warp's list in shared memory.
 //  3. Up to 32 candidates (about topk + a few for smooth logits) are ranked
-//     by one warp sort; more, by topk rounds of a warp argmax as in
-//     topk_rows_kernel, with the same whole-row fallback when they overflow.
-// topk <= 32.  Grid rows; gmax[row][groups], group g = elements [32 g, 32 g + 32).
-__global__ void __launch_bounds__(kRowThreads)
+//     by one warp sort, up to kGroupCand by topk warp-argmax rounds over the
+//     list; more (many equal values) by topk rounds over the qualifying
+//     groups themselves.
+// topk <= 32.  gmax[row][groups], groups a multiple of 4 (16-byte rows), group
+// g = elements [32 g, 32 g + 32) of x[row][n].
+constexpr int kGroupWarps = 8;  // rows per CTA
+constexpr int kGroupCand = 64;  // candidates a warp keeps
+constexpr int kGroupRegs = 8;   // 16-byte group-maxima loads a lane keeps in registers
+
+__device__ __forceinline__ float f4_at(const float4& q, int u) {
+  return u == 0 ? q.x : u == 1 ? q.y : u == 2 ? q.z : q.w;
+}
+
+// The 32 elements of group g of row xr (n elements), eight 16-byte loads in flight when aligned.
+__device__ __forceinline__ void load_group(const float* __restrict__ xr, int n, bool vec, int g, float (&v)[32]) {
+  const int e0 = 32 * g;
+  if (vec && e0 + 32 <= n) {
+    float4 q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) q[k] = reinterpret_cast<const float4*>(xr + e0)[k];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[4 * k] = q[k].x;
+      v[4 * k + 1] = q[k].y;
+      v[4 * k + 2] = q[k].z;
+      v[4 * k + 3] = q[k].w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = e0 + k < n ? xr[e0 + k] : -INFINITY;
+  }
+}
+
+__global__ void __launch_bounds__(32 * kGroupWarps)
 topk_groups_kernel(const float* __restrict__ x, const float* __restrict__ gmax, int n, int groups, int topk,
-                   float* __restrict__ out_v, int* __restrict__ out_i) {
-  __shared__ float cv[kRowCap];
-  __shared__ int ci[kRowCap];
-  __shared__ float sv[kRowThreads / 32];
-  __shared__ int si[kRowThreads / 32];
-  __shared__ int s_count;
+                   int rows, float* __restrict__ out_v, int* __restrict__ out_i) {
+  __shared__ float cv[kGroupWarps][kGroupCand];
+  __shared__ int ci[kGroupWarps][kGroupCand];
+  __shared__ int cnt[kGroupWarps];
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kGroupWarps + warp;
+  if (row >= rows) return;  // the warps are independent: no block barrier follows
   const float* xr = x + (size_t)row * n;
-  const float* gr = gmax + (size_t)row * groups;
-  constexpr int GU = 4;  // group maxima a thread has in flight
-  // 1. thread bests over the group maxima
-  float mv = -INFINITY;
-  int mg = INT_MAX;
-  for (int g0 = tid; g0 < groups; g0 += kRowThreads * GU) {
-    float t[GU];
-#pragma unroll
-    for (int u = 0; u < GU; ++u) {
-      const int g = g0 + u * kRowThreads;
-      t[u] = g < groups ? gr[g] : -INFINITY;
-    }
-#pragma unroll
-    for (int u = 0; u < GU; ++u) {
-      const int g = g0 + u * kRowThreads;
-      if (g < groups && ranks_ahead(t[u], g, mv, mg)) { mv = t[u]; mg = g; }
-    }
-  }
-  cv[tid] = mv;
-  ci[tid] = mg;
-  __syncthreads();
-  if (tid < 32) {
-    // lane best over threads lane, lane + 32, ...; then topk rounds of a warp
-    // argmax over the 32 lane bests, the winner dropping out each round
-    float lv = cv[lane];
-    int lg = ci[lane];
-#pragma unroll
-    for (int w = 1; w < kRowThreads / 32; ++w)
-      if (ranks_ahead(cv[lane + 32 * w], ci[lane + 32 * w], lv, lg)) { lv = cv[lane + 32 * w]; lg = ci[lane + 32 * w]; }
-    warp_sort32(lv, lg);
-    const float T = __shfl_sync(0xffffffffu, lv, topk - 1);
-    if (lane == 0) { sv[0] = T; s_count = 0; }
-  }
-  __syncthreads();
-  const float T = sv[0];
-  // 2. elements >= T of the groups that reach T
+  const float4* g4 = reinterpret_cast<const float4*>(gmax + (size_t)row * groups);
+  const int chunks = groups >> 2;  // 4 groups per 16-byte chunk; lane takes chunks lane + 32 j
+  const bool in_regs = chunks <= 32 * kGroupRegs;
   const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15u) == 0;
-  auto take = [&](float v, int i) {
-    if (v >= T) {
-      const int slot = atomicAdd(&s_count, 1);
-      if (slot < kRowCap) { cv[slot] = v; ci[slot] = i; }
-    }
-  };
-  for (int g0 = tid; g0 < groups; g0 += kRowThreads * GU) {
-    float t[GU];
+  float4 gm[kGroupRegs];
+  // 1. lane best over its groups
+  float lv = -INFINITY;
+  int lg = INT_MAX;
+#pragma unroll 1
+  for (int c0 = lane; c0 < chunks; c0 += 32 * kGroupRegs) {
 #pragma unroll
-    for (int u = 0; u < GU; ++u) {
-      const int g = g0 + u * kRowThreads;
-      t[u] = g < groups ? gr[g] : -INFINITY;
+    for (int r = 0; r < kGroupRegs; ++r) {
+      const int c = c0 + 32 * r;
+      gm[r] = c < chunks ? g4[c] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int u = 0; u < GU; ++u) {
-      const int g = g0 + u * kRowThreads;
-      if (g >= groups || !(t[u] >= T)) continue;
-      const int e0 = 32 * g;
-      if (vec && e0 + 32 <= n) {
-        float4 q4[8];
+    for (int r = 0; r < kGroupRegs; ++r)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) q4[q] = reinterpret_cast<const float4*>(xr + e0)[q];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          take(q4[q].x, e0 + 4 * q);
-          take(q4[q].y, e0 + 4 * q + 1);
-          take(q4[q].z, e0 + 4 * q + 2);
-          take(q4[q].w, e0 + 4 * q + 3);
-        }
-      } else {
-        for (int i = e0; i < e0 + 32 && i < n; ++i) take(xr[i], i);
+      for (int u = 0; u < 4; ++u) {
+        const int g = 4 * (c0 + 32 * r) + u;
+        if (c0 + 32 * r < chunks && ranks_ahead(f4_at(gm[r], u), g, lv, lg)) { lv = f4_at(gm[r], u); lg = g; }
       }
-    }
   }
-  __syncthreads();
-  const int c = s_count;
-  // 3. at most 32 candidates (the usual case): one warp sort, ranks 0 .. topk-1
-  // in lanes 0 .. topk-1; more: topk rounds, each the best candidate ranked
-  // behind the previous winner
-  if (c <= 32) {
-    if (tid < 32) {
-      float v = tid < c ? cv[tid] : -INFINITY;
-      int id = tid < c ? ci[tid] : INT_MAX;
-      warp_sort32(v, id);
-      if (tid < topk) {
-        out_v[(size_t)row * topk + tid] = v;
-        out_i[(size_t)row * topk + tid] = id;
-      }
+  // 2. T = the topk-th best lane best
+  float tv = lv;
+  int ti = lg;
+  warp_sort32(tv, ti);
+  const float T = __shfl_sync(0xffffffffu, tv, topk - 1);
+  // 3. this lane's groups whose maximum reaches T: their elements >= T go to the warp's list
+  if (lane == 0) cnt[warp] = 0;
+  __syncwarp();
+  // the j-th (0-based) group of this lane reaching T, or -1
+  auto qualifying = [&](int j) -> int {
+    int seen = 0;
+    if (in_regs) {
+#pragma unroll
+      for (int r = 0; r < kGroupRegs; ++r)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = lane + 32 * r;
+          if (c < chunks && f4_at(gm[r], u) >= T && seen++ == j) return 4 * c + u;
+        }
+      return -1;
     }
+    for (int c = lane; c < chunks; c += 32) {
+      const float4 q = g4[c];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (f4_at(q, u) >= T && seen++ == j) return 4 * c + u;
+    }
+    return -1;
+  };
+#pragma unroll 1
+  for (int j = 0;; ++j) {
+    const int g = qualifying(j);
+    if (g < 0) break;
+    float v[32];
+    load_group(xr, n, vec, g, v);
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (v[k] >= T) {
+        const int slot = atomicAdd(&cnt[warp], 1);
+        if (slot < kGroupCand) { cv[warp][slot] = v[k]; ci[warp][slot] = 32 * g + k; }
+      }
+  }
+  __syncwarp();
+  const int c = cnt[warp];
+  float* wv = out_v + (size_t)row * topk;
+  int* wi = out_i + (size_t)row * topk;
+  if (c <= 32) {
+    float v = lane < c ? cv[warp][lane] : -INFINITY;
+    int id = lane < c ? ci[warp][lane] : INT_MAX;
+    warp_sort32(v, id);
+    if (lane < topk) { wv[lane] = v; wi[lane] = id; }
     return;
   }
   float pv = INFINITY;
   int pi = -1;
-  if (c <= kRowCap) {
-    if (tid < 32) {
-      for (int r = 0; r < topk; ++r) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int j = tid; j < c; j += 32)
-          if (ranks_ahead(pv, pi, cv[j], ci[j]) && ranks_ahead(cv[j], ci[j], bv, bi)) { bv = cv[j]; bi = ci[j]; }
-        warp_best(bv, bi);
-        if (tid == 0) {
-          out_v[(size_t)row * topk + r] = bv;
-          out_i[(size_t)row * topk + r] = bi;
-        }
-        pv = bv;
-        pi = bi;
-      }
-    }
-    return;
-  }
+#pragma unroll 1
   for (int r = 0; r < topk; ++r) {
     float bv = -INFINITY;
     int bi = INT_MAX;
-    for (int i = tid; i < n; i += kRowThreads) {
-      const float v = xr[i];
-      if (ranks_ahead(pv, pi, v, i) && ranks_ahead(v, i, bv, bi)) { bv = v; bi = i; }
+    if (c <= kGroupCand) {
+      for (int k = lane; k < c; k += 32)
+        if (ranks_ahead(pv, pi, cv[warp][k], ci[warp][k]) && ranks_ahead(cv[warp][k], ci[warp][k], bv, bi)) {
+          bv = cv[warp][k];
+          bi = ci[warp][k];
+        }
+    } else {
+      // many values reach T (ties): rank the qualifying groups' elements directly
+#pragma unroll 1
+      for (int j = 0;; ++j) {
+        const int g = qualifying(j);
+        if (g < 0) break;
+        float v[32];
+        load_group(xr, n, vec, g, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (ranks_ahead(pv, pi, v[k], 32 * g + k) && ranks_ahead(v[k], 32 * g + k, bv, bi)) {
+            bv = v[k];
+            bi = 32 * g + k;
+          }
+      }
     }
-    block_best(bv, bi, sv, si);
-    if (tid == 0) {
-      out_v[(size_t)row * topk + r] = bv;
-      out_i[(size_t)row * topk + r] = bi;
-    }
+    warp_best(bv, bi);
+    if (lane == 0) { wv[r] = bv; wi[r] = bi; }
     pv = bv;
     pi = bi;
   }
@@ -903,8 +921,8 @@ extern "C" medusa_status medusa_heads(const void* h, const void* w1, const void*
                                     gm, d_status, s);
     if (st != MEDUSA_OK) return st;
     // one ranking kernel, reading only the groups that can hold a top-k logit
-    launch_pdl(topk_groups_kernel, dim3(B * K), dim3(kRowThreads), 0, s, (const float*)z, (const float*)gm, V,
-               heads_tc_groups(V), topk, topk_logit, topk_idx);
+    launch_pdl(topk_groups_kernel, dim3(ceil_div(B * K, kGroupWarps)), dim3(32 * kGroupWarps), 0, s, (const float*)z,
+               (const float*)gm, V, heads_tc_groups(V), topk, B * K, topk_logit, topk_idx);
     return launch_status();
   }
   WsCarver wc(ws);
