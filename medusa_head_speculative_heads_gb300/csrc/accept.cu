@@ -86,6 +86,72 @@ node_partial_kernel(const float* __restrict__ logits, int N, int V, int C, float
   pdl_trigger();
   const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
 
+  // Chunks of at most kPartThreads x 16 values (V up to 65536): the chunk
+  // stays in registers between the max and the sums (16-byte loads all in
+  // flight, one memory pass) and the warps meet twice in shared memory.
+  constexpr int kRegQ = 4;  // float4 per thread
+  if (vec && hi - lo <= kPartThreads * 4 * kRegQ) {
+    __shared__ float4 wsum[kPartThreads / 32];
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+    float4 q[kRegQ];
+#pragma unroll
+    for (int k = 0; k < kRegQ; ++k) {
+      const int qi = (lo >> 2) + tid + k * kPartThreads;
+      q[k] = qi < (hi >> 2) ? z4[qi] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    float mv = -INFINITY;
+    int mi = INT_MAX;
+#pragma unroll
+    for (int k = 0; k < kRegQ; ++k) {
+      const int qi = (lo >> 2) + tid + k * kPartThreads;
+      const float e[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (qi < (hi >> 2) && ranks_ahead(e[j], 4 * qi + j, mv, mi)) { mv = e[j]; mi = 4 * qi + j; }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, mv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, mi, o);
+      if (ranks_ahead(v2, i2, mv, mi)) { mv = v2; mi = i2; }
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    if (lane == 0) { sv[warp] = mv; si[warp] = mi; }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kPartThreads / 32; ++w)
+      if (ranks_ahead(sv[w], si[w], mv, mi)) { mv = sv[w]; mi = si[w]; }
+    float S = 0.f, E = 0.f;
+    if (T > 0.f && lo < hi) {
+      const float inv_t = 1.f / T;
+      float s2 = 0.f, e2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < kRegQ; ++k) {
+        const int qi = (lo >> 2) + tid + k * kPartThreads;
+        if (qi >= (hi >> 2)) continue;
+        const float x[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = (x[j] - mv) * inv_t;
+          const float w = expf(a);
+          s2 += w;
+          e2 = fmaf(w, a, e2);
+        }
+      }
+      s2 = warp_sum(s2);
+      e2 = warp_sum(e2);
+      if (lane == 0) wsum[warp] = make_float4(s2, e2, 0.f, 0.f);
+      __syncthreads();
+      if (tid == 0)
+        for (int w = 0; w < kPartThreads / 32; ++w) {
+          S += wsum[w].x;
+          E += wsum[w].y;
+        }
+    }
+    if (tid == 0) part[((size_t)b * N + n) * C + c] = make_float4(mv, __int_as_float(mi), S, E);
+    return;
+  }
+
   float mv = -INFINITY;
   int mi = INT_MAX;
   if (vec) {
