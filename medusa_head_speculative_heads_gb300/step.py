@@ -126,11 +126,14 @@ class PipelinedSteps:
     """Verify steps fed from host memory, with the host->device copy of the
     next step's inputs overlapping the current step's kernels.
 
-    Two device copies of the per-step inputs alternate: step i runs (as a
+    `n_sets` device copies of the per-step inputs rotate: step i runs (as a
     captured graph, followed by the device->host read of its results) on the
-    compute stream from set i % 2 while a copy stream uploads step i + 1's
-    inputs into the other set, which step i - 1 has finished reading.  Model
-    state (weights, KV cache) stays resident and is shared by both sets.
+    compute stream from set i % n_sets while a copy stream uploads the next
+    steps' inputs into the other sets, each once the step that last used it
+    has finished reading it (with three sets the uploads can run two steps
+    ahead; measured no faster than two at the 7B shape, where the host link
+    bounds the copies).
+    Model state (weights, KV cache) stays resident and is shared by all sets.
 
     Each device set is one buffer holding the inputs at fixed 256-byte aligned
     offsets, so a step whose inputs are staged in the matching pinned host
@@ -146,9 +149,12 @@ class PipelinedSteps:
 
     names = ("h", "root_tok", "prefix_len", "q", "kt", "vt", "logits")
 
-    def __init__(self, vs: VerifyStep, dev_inputs: dict, resident: dict, outs, host_outs):
+    def __init__(self, vs: VerifyStep, dev_inputs: dict, resident: dict, outs, host_outs, n_sets: int = 2):
         import torch
+        if n_sets < 2:
+            raise ValueError("n_sets must be at least 2")
         self.vs = vs
+        self.n_sets = n_sets
         self.layout = []  # (name, offset, nbytes, dtype, shape)
         off = 0
         for k in self.names:
@@ -158,15 +164,15 @@ class PipelinedSteps:
             off += (nb + 255) // 256 * 256
         self.total = off
         dev = dev_inputs[self.names[0]].device
-        self.bufs = [torch.empty(self.total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.bufs = [torch.empty(self.total, dtype=torch.uint8, device=dev) for _ in range(n_sets)]
         self.sets = [self._views(b) for b in self.bufs]
         for st in self.sets:
             for k in self.names:
                 st[k].copy_(dev_inputs[k])
         self.outs, self.host_outs = list(outs), list(host_outs)
         self.copy_stream = torch.cuda.Stream()
-        self.copied = [torch.cuda.Event(), torch.cuda.Event()]
-        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.copied = [torch.cuda.Event() for _ in range(n_sets)]
+        self.done = [torch.cuda.Event() for _ in range(n_sets)]
         self.last_h2d = 0
         r = resident
 
@@ -201,14 +207,14 @@ class PipelinedSteps:
         host_staging() (one copy) or a dict of tensors (one copy each).  No host
         synchronisation."""
         import torch
-        s = self.i % 2
+        s = self.i % self.n_sets
         main = torch.cuda.current_stream()
         cs = self.copy_stream
         if self.i == 0:
             cs.wait_stream(main)  # a new sequence starts after everything enqueued so far
         with torch.cuda.stream(cs):
-            if self.i >= 2:
-                cs.wait_event(self.done[s])  # step i - 2 has finished reading this set
+            if self.i >= self.n_sets:
+                cs.wait_event(self.done[s])  # step i - n_sets has finished reading this set
             if isinstance(host_inputs, dict):
                 for k in self.names:
                     self.sets[s][k].copy_(host_inputs[k], non_blocking=True)

@@ -44,10 +44,12 @@ def _verify_step(mg, c):
                       temperature=c["T"], eps=c["eps"], delta=c["delta"])
 
 
-def test_pipelined_steps_match_sequential_steps(mg):
+@pytest.mark.parametrize("n_sets", [2, 3])
+def test_pipelined_steps_match_sequential_steps(mg, n_sets):
+    """Each device input set is reused (five steps over two or three sets)."""
     from medusa_head_speculative_heads_gb300.step import PipelinedSteps
     c = wl.config("tiny")
-    steps = _steps(c, 4)
+    steps = _steps(c, 5)
     w1, w2 = to_dev(steps[0]["w1"]), to_dev(steps[0]["w2"])
 
     # one step after another (eager, no overlap)
@@ -68,7 +70,7 @@ def test_pipelined_steps_match_sequential_steps(mg):
     outs = [vs2.accept_len, vs2.path_nodes, vs2.next_tok, vs2.new_len]
     host_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     pipe = PipelinedSteps(vs2, {k: to_dev(steps[0][k]) for k in PER_STEP}, dict(w1=w1, w2=w2, kc=kc2, vc=vc2),
-                          outs, host_outs)
+                          outs, host_outs, n_sets=n_sets)
     hosts = [{k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory() for k in PER_STEP} for inp in steps]
     pipe.reset()
     for hst in hosts:
