@@ -244,8 +244,13 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
   pdl_wait();
   pdl_trigger();
   if (tid == 0) s_bad = 0;
-  // the topology of node c, loaded with the partials below (one round trip)
+  // the topology and token of node c, loaded with the partials below (one
+  // round trip), then the logit of that token under its parent's distribution
+  // (the second round trip overlaps the combination of the partials)
   const int dc_ld = c < N ? depth[c] : -1, pc_ld = c < N ? parent[c] : -1;
+  const int x_ld = (c > 0 && c < N) ? tokens[(size_t)b * N + c] : -1;
+  const bool z_ok = c > 0 && c < N && pc_ld >= 0 && pc_ld < N && x_ld >= 0 && x_ld < V;
+  const float z_px = z_ok ? logits[((size_t)b * N + pc_ld) * V + x_ld] : 0.f;
   // 1. statistics of every node: grp threads per node, strided over the chunks
   {
     const int node = tid / grp, sub = tid % grp;
@@ -315,14 +320,14 @@ select_path_kernel(const float* __restrict__ logits, const int32_t* __restrict__
     int ok = 1;
     float p = 1.f, t = 0.f;
     if (c > 0) {
-      const int x = tokens[(size_t)b * N + c];
+      const int x = x_ld;
       t = thr[pc];
       if (x < 0 || x >= V) {
         set_status(d_status, MEDUSA_DEV_BAD_INDEX);
         ok = 0;
         p = 0.f;
       } else if (T > 0.f) {
-        p = expf((logits[((size_t)b * N + pc) * V + x] - zmax[pc]) / T) / ssum[pc];
+        p = expf((z_px - zmax[pc]) / T) / ssum[pc];
         ok = p > t;
       } else {
         ok = x == amax[pc];
