@@ -55,6 +55,9 @@ def _tau(dtype):
     # top-32 on the tensor-core path: 33 to 64 candidates usually reach the
     # ranking threshold (the warp-argmax rounds instead of one warp sort)
     dict(name="tiny", dtype="bf16", B=6, H=512, V=12000, K=2, topk=32),
+    # more than 32768 logits per row: the ranking reads its group maxima in
+    # rounds instead of holding them in registers
+    dict(name="tiny", dtype="bf16", B=4, H=256, V=40000, K=2, topk=10),
 ], ids=lambda c: f"{c.get('dtype', 'f32')}-B{c.get('B', 1)}-H{c.get('H', 256)}-V{c.get('V', 1024)}")
 def test_heads_parity(mg, case):
     c = wl.config(**case)
@@ -391,6 +394,19 @@ def test_typical_accept_tiny_config_and_dense_tree(mg):
     tokens = wl.random_tokens(c, t.n_nodes)
     logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=0.8)
     _accept_case(mg, c, t, tokens, logits, 0.8, 0.09, 0.3)
+
+
+@pytest.mark.parametrize("V", [65536, 152064])
+def test_typical_accept_large_vocabulary(mg, V):
+    """Vocabularies at and past the size whose acceptance chunks (at most 32 per
+    node) still fit the per-thread registers: 152064 (a Qwen-size vocabulary)
+    takes the two-pass chunk path."""
+    c = wl.config("tiny", V=V, B=2)
+    t = otopo.greedy(otopo.synthetic_accuracy(3, 4), 16)
+    tokens = wl.random_tokens(c, t.n_nodes)
+    logits = wl.plant(c, wl.base_logits(c, t.n_nodes), tokens, t.parent, prob=0.7)
+    _, _, differs = _accept_case(mg, c, t, tokens, logits, 0.7, 0.09, 0.3)
+    assert differs == 0
 
 
 def test_typical_accept_bad_token_reports(mg):
