@@ -52,7 +52,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the barrier phase with the given parity.  Gives up (returns
 // false) when *abort becomes non-zero or after `limit_ns`; on a timeout it
-// raises *abort itself.
+// raises *abort itself.  The elapsed time is a signed difference: should the
+// global timer step back (it is kept in step with the host clock), the wait
+// goes on instead of ending at once.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -60,7 +62,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
+    if ((int64_t)(global_timer_ns() - t0) > (int64_t)limit_ns) {
       if (abort) *abort = 1;
       return false;
     }
