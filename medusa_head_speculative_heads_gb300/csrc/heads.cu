@@ -173,12 +173,13 @@ __device__ __forceinline__ void warp_merge_sorted(const float* v, const int* idx
 //                 cand_{v,i}[(b*K + k) * gridDim.x + blockIdx.x][topk].
 // Grid (ctas_per_head, K); block 256; dynamic smem BB * C floats (+ BB * cap
 // floats holding the CTA's logits for the ranking).
-// One vector (the decode case), measured per step: the W1 pass runs five CTAs
-// per SM (48 registers; a few spill outside the row loop) and the W2 pass is
-// left to the compiler (80 registers, no spills, three CTAs per SM).  Both at
-// five: W2 spilled and the step was 7.5 us slower; both at six: far slower.
+// One vector (the decode case), measured per step: the W1 pass runs four CTAs
+// per SM (64 registers, no spills; five CTAs at 48 registers spilled and the
+// step was ~0.7 % slower) and the W2 pass is left to the compiler (80
+// registers, no spills, three CTAs per SM).  Both at five: W2 spilled and the
+// step was 7.5 us slower; both at six: far slower.
 template <typename TW, int BB, bool kFirst>
-__global__ void __launch_bounds__(kGemvThreads, BB == 1 && kFirst ? 5 : 1)
+__global__ void __launch_bounds__(kGemvThreads, BB == 1 && kFirst ? 4 : 1)
 heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const float* __restrict__ u,
                   int B, int b0, int K, int rows_per_head, int C, float* __restrict__ out, int topk,
                   float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters,
