@@ -18,8 +18,9 @@
 //
 // Roles (256 threads, one CTA per SM, persistent over 128-row tiles): warp 0
 // lane 0 issues TMA loads of the A (weights) and B (vector) tiles into a ring
-// of 7 to 11 stages (the smaller the batch, the smaller the B tile and the
-// more weight bytes in flight); warp 1 allocates TMEM and lane 0 issues the
+// sized per pass (the smaller the B tile, the more weight bytes in flight: W2
+// 7 to 11 stages, W1, whose B tile has no lo rows, 9 to 12); warp 1 allocates
+// TMEM and lane 0 issues the
 // MMAs (four K=16 steps per 64-column stage) into one of two accumulators;
 // warps 4-7 read the accumulator (one row per thread) and write the outputs,
 // so the epilogue of one tile overlaps the main loop of the next.  The W1
@@ -43,10 +44,11 @@ constexpr int kMaxStages = 12;
 constexpr uint32_t kATile = 16384;  // 128 rows x 128 bytes
 constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
 
-// Ring geometry for a padded batch BP: the B tile holds 2 BP rows of 128 bytes.
-template <int BP>
+// Ring geometry for a padded batch BP and a pass: the B tile holds BP rows of
+// 128 bytes in the W1 pass (h) and 2 BP rows in the W2 pass (u, hi and lo).
+template <int BP, bool W1>
 struct Ring {
-  static constexpr uint32_t kStageBytes = kATile + 256u * BP;
+  static constexpr uint32_t kStageBytes = kATile + 128u * (W1 ? BP : 2 * BP);
   static constexpr int kStages = (int)(224u * 1024u / kStageBytes) < kMaxStages ? (int)(224u * 1024u / kStageBytes)
                                                                                  : kMaxStages;
   static constexpr uint32_t kOffBar = kStages * kStageBytes;
@@ -62,7 +64,6 @@ struct Params {
   int K, R, H, B, Bp, N;  // R rows per head, N = 2 * Bp (rows of u2 per head)
   int mma_n;              // columns of the product: N (W2: hi and lo rows), Bp (W1: h is exact in bf16)
   int tiles_per_head, tiles;
-  int first;              // 1: W1 pass, 0: W2 pass
   int next_R, next_tiles_per_head, next_tiles;  // W1 pass: the W2 pass's geometry (its first boxes go to L2)
   const uint16_t* h;      // [B][H] bf16 (W1 residual)
   uint16_t* u2;           // [K][N][H] bf16, W1 output (hi rows, then lo rows)
@@ -114,15 +115,15 @@ __device__ __forceinline__ void warp_colmax(float (&a)[N], int lane) {
 
 }  // namespace htc
 
-template <int BP>
+template <int BP, bool W1>
 __global__ void __launch_bounds__(htc::kThreads, 1)
 heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_next, const htc::Params p) {
   constexpr int NC = 2 * BP;  // accumulator columns
   using namespace htc;
-  constexpr int kStages = Ring<BP>::kStages;
-  constexpr uint32_t kStageBytes = Ring<BP>::kStageBytes;
-  constexpr uint32_t kOffBar = Ring<BP>::kOffBar;
+  constexpr int kStages = Ring<BP, W1>::kStages;
+  constexpr uint32_t kStageBytes = Ring<BP, W1>::kStageBytes;
+  constexpr uint32_t kOffBar = Ring<BP, W1>::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
@@ -169,11 +170,13 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         tma_prefetch_l2_2d(&tm_a, kk * 64, k * p.R + m0);
       }
     }
-    if (p.first && (int)blockIdx.x < p.next_tiles) {
+    if (W1 && (int)blockIdx.x < p.next_tiles) {
       const int tile = blockIdx.x;
       const int k = tile / p.next_tiles_per_head, m0 = (tile % p.next_tiles_per_head) * 128;
-      const int hi = n + kNextBoxes < ksteps ? n + kNextBoxes : ksteps;
-      for (int i = n; i < hi; ++i) {
+      constexpr int kNextStages = Ring<BP, false>::kStages;
+      const int lo = kNextStages < ksteps ? kNextStages : ksteps;
+      const int hi = lo + kNextBoxes < ksteps ? lo + kNextBoxes : ksteps;
+      for (int i = lo; i < hi; ++i) {
         const int kk = i + k_rot < ksteps ? i + k_rot : i + k_rot - ksteps;
         tma_prefetch_l2_2d(&tm_next, kk * 64, k * p.next_R + m0);
       }
@@ -204,7 +207,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
           uint8_t* st = smem + s * kStageBytes;
           mbar_expect_tx(&bars->full[s], kATile + b_bytes);
           tma_load_2d_hint(st, &tm_a, &bars->full[s], kk * 64, k * p.R + m0, once);
-          tma_load_2d(st + kATile, &tm_b, &bars->full[s], kk * 64, p.first ? 0 : k * p.N);
+          tma_load_2d(st + kATile, &tm_b, &bars->full[s], kk * 64, W1 ? 0 : k * p.N);
         }
       }
       if (!alive)
@@ -254,7 +257,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       const int ab = tc & 1;
       // W1: this row's residual h[b][row] (bf16 pairs), loaded while the MMAs run.
       uint32_t hres[BP / 2];
-      if (p.first) {
+      if (W1) {
         const int row = (tile % p.tiles_per_head) * 128 + m;
 #pragma unroll
         for (int b2 = 0; b2 < BP / 2; ++b2) {
@@ -267,7 +270,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       tc_fence_after();
       // W1 products have BP columns (no lo part), W2 products 2 BP.
       float v[NC];
-      if (p.first) {
+      if (W1) {
 #pragma unroll
         for (int c = 0; c < BP / 8; ++c) tmem_ld8(lane_addr + ab * 128 + c * 8, v + c * 8);
       } else {
@@ -278,7 +281,7 @@ heads_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars->acc_empty[ab]);
       const int k = tile / p.tiles_per_head, row = (tile % p.tiles_per_head) * 128 + m;
-      if (p.first) {
+      if (W1) {
         if (row >= p.R) continue;
 #pragma unroll
         for (int b = 0; b < BP; ++b) {
@@ -368,6 +371,19 @@ bool heads_tc_supported(int B, int H, const void* h, const void* w1, const void*
          heads_encode_fn() != nullptr;
 }
 
+// The instantiation of one pass for a padded batch, with its shared memory.
+struct heads_tc_pass {
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, htc::Params);
+  uint32_t smem;
+};
+template <bool W1>
+static heads_tc_pass heads_tc_pick(int Bp) {
+  if (Bp == 16) return {heads_tc_kernel<16, W1>, htc::Ring<16, W1>::kSmemBytes};
+  if (Bp == 32) return {heads_tc_kernel<32, W1>, htc::Ring<32, W1>::kSmemBytes};
+  if (Bp == 48) return {heads_tc_kernel<48, W1>, htc::Ring<48, W1>::kSmemBytes};
+  return {heads_tc_kernel<64, W1>, htc::Ring<64, W1>::kSmemBytes};
+}
+
 // Both passes: u2 = split(SiLU(W1 h) + h) ([K][2Bp][H] bf16, caller scratch),
 // then z = W2 u ([B][K][V] fp32) and the maximum of every 32-row group of z
 // ([B][K][4 ceil(V / 128)] fp32, groups past V hold -inf).
@@ -378,13 +394,9 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   if (!map_rows(&ma1, w1, H, (long long)K * H, 128) || !map_rows(&mb1, h, H, B, Bp) ||
       !map_rows(&ma2, w2, H, (long long)K * V, 128) || !map_rows(&mb2, u2, H, (long long)K * N, N))
     return MEDUSA_ERR_CUDA;
-  auto kern = Bp == 16 ? heads_tc_kernel<16> : Bp == 32 ? heads_tc_kernel<32> : Bp == 48 ? heads_tc_kernel<48>
-                                                                                 : heads_tc_kernel<64>;
-  const uint32_t smem = Bp == 16   ? htc::Ring<16>::kSmemBytes
-                        : Bp == 32 ? htc::Ring<32>::kSmemBytes
-                        : Bp == 48 ? htc::Ring<48>::kSmemBytes
-                                   : htc::Ring<64>::kSmemBytes;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  const heads_tc_pass k1 = heads_tc_pick<true>(Bp), k2 = heads_tc_pick<false>(Bp);
+  if (cudaFuncSetAttribute(k1.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k1.smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k2.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k2.smem) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
   const int sms = device_sm_count();
   // Equal-cost tiles: as many rounds as the SM count forces, spread evenly.
@@ -405,21 +417,19 @@ medusa_status heads_tc_run(const uint16_t* h, const uint16_t* w1, const uint16_t
   p.d_status = d_status;
   // W1: rows per head = H
   p.R = H;
-  p.first = 1;
   p.mma_n = Bp;
   p.tiles_per_head = ceil_div(H, 128);
   p.tiles = K * p.tiles_per_head;
   p.next_R = V;
   p.next_tiles_per_head = ceil_div(V, 128);
   p.next_tiles = grid_for(K * p.next_tiles_per_head);  // the W2 CTAs' first tiles
-  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma1, mb1, ma2, p);
+  launch_pdl(k1.kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), k1.smem, s, ma1, mb1, ma2, p);
   // W2: rows per head = V
   p.R = V;
-  p.first = 0;
   p.mma_n = N;
   p.tiles_per_head = ceil_div(V, 128);
   p.tiles = K * p.tiles_per_head;
-  launch_pdl(kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), smem, s, ma2, mb2, ma2, p);
+  launch_pdl(k2.kern, dim3(grid_for(p.tiles)), dim3(htc::kThreads), k2.smem, s, ma2, mb2, ma2, p);
   return launch_status();
 }
 
