@@ -302,6 +302,11 @@ def run_profile(args, c, mg, topo, dev):
         vs.heads(d["h"], d["w1"], d["w2"], stream)
         vs.tree(d["root_tok"], d["prefix_len"], stream)
         torch.cuda.synchronize()
+        # The planting indexes the logits with the tree tokens on the device:
+        # check them on the host first (an out-of-range index there is a
+        # device-side assertion, not an exception).
+        if vs.check() != 0 or not bool(((vs.tokens >= 0) & (vs.tokens < c["V"])).all()):
+            raise RuntimeError("tree tokens outside the vocabulary")
         plant_on_device(c, d["logits"], vs.tokens, np.asarray(topo.parent))
         call = {"heads": lambda: vs.heads(d["h"], d["w1"], d["w2"], stream),
                 "attention": lambda: vs.attention(d["q"], d["kc"], d["vc"], d["kt"], d["vt"], d["prefix_len"],
@@ -617,6 +622,8 @@ def plant_on_device(c, logits, tokens, parent):
     ni_t = torch.from_numpy(ni).to(logits.device)
     ch_t = torch.from_numpy(first[ni]).to(logits.device)
     tok = tokens[bi_t, ch_t].long()
+    if not bool(((tok >= 0) & (tok < V)).all()):
+        raise RuntimeError("planting: tree tokens outside the vocabulary")
     rowmax = logits[bi_t, ni_t].amax(dim=1)
     logits[bi_t, ni_t, tok] = rowmax + 4.0
 
