@@ -58,6 +58,12 @@ def _tau(dtype):
     # more than 32768 logits per row: the ranking reads its group maxima in
     # rounds instead of holding them in registers
     dict(name="tiny", dtype="bf16", B=4, H=256, V=40000, K=2, topk=10),
+    # one vector (the decode case) at more CTAs per head than the W2 pass's
+    # in-kernel merge holds (the candidate lists then go through the ranking
+    # kernels), top-32 and odd sizes
+    dict(name="tiny", dtype="bf16", B=1, H=4096, V=5000, K=4, topk=32),
+    dict(name="tiny", dtype="bf16", B=1, H=512, V=12000, K=1, topk=10),
+    dict(name="tiny", dtype="f32", B=1, H=264, V=2049, K=3, topk=20),
 ], ids=lambda c: f"{c.get('dtype', 'f32')}-B{c.get('B', 1)}-H{c.get('H', 256)}-V{c.get('V', 1024)}")
 def test_heads_parity(mg, case):
     c = wl.config(**case)
@@ -143,6 +149,30 @@ def test_heads_batch_ranking_exact_ties(mg, distinct):
     Bit-exact against the oracle, ties ranked by index."""
     B, H, V, K, topk = 8, 1024, 8000, 2, 10
     g = np.random.default_rng(11 + distinct)
+    h = wl.to_bf16_bits((np.clip(np.round(g.standard_normal((B, H)) * 8), -32, 32) / 8).astype(np.float32))
+    w1 = np.zeros((K, H, H), np.uint16)
+    base = g.integers(-1, 2, size=(K, distinct, H)).astype(np.float32)
+    w2 = wl.to_bf16_bits(base[:, np.arange(V) % distinct, :])
+    ref = oracle.heads(h, w1, w2, topk)
+    st = _status(mg)
+    idx, val = mg.medusa_heads(to_dev(h), to_dev(w1), to_dev(w2), topk, d_status=st)
+    torch.cuda.synchronize()
+    assert mg.medusa_status_check(st) == 0
+    np.testing.assert_array_equal(to_host(idx), ref["idx"])
+    np.testing.assert_array_equal(to_host(val).astype(np.float64), ref["val"])
+
+
+@pytest.mark.parametrize("H,K,V,distinct", [(1024, 2, 8000, 2), (4096, 4, 4000, 100)])
+def test_heads_one_vector_ranking_exact_ties(mg, H, K, V, distinct):
+    """One vector (B = 1) on logits exact in fp32 in any summation order
+    (W1 = 0, h in multiples of 1/8, W2 rows in {-1, 0, 1}, `distinct`
+    different rows tiled over the vocabulary): with two distinct rows every
+    CTA's candidate list is one tied value (more CTAs per head than the W2
+    pass's own merge holds: the lists go through the ranking kernels); with
+    100 the best value repeats 40 times across the CTAs that the last CTA of
+    each head merges.  Bit-exact against the oracle, ties ranked by index."""
+    B, topk = 1, 10
+    g = np.random.default_rng(23 + distinct)
     h = wl.to_bf16_bits((np.clip(np.round(g.standard_normal((B, H)) * 8), -32, 32) / 8).astype(np.float32))
     w1 = np.zeros((K, H, H), np.uint16)
     base = g.integers(-1, 2, size=(K, distinct, H)).astype(np.float32)
