@@ -129,6 +129,92 @@ __device__ __forceinline__ void warp_topk(const float* v, const int* idx, int n,
   }
 }
 
+// warp_topk with the values held in registers: lane l keeps v[l + 32 j],
+// j < RV (n <= 32 RV), read from shared memory once, so a round is register
+// compares and the shuffle argmax, not a pass of dependent shared-memory
+// reads.  Same ranking and output as warp_topk (idx null: index base + i).
+template <int RV>
+__device__ __forceinline__ void warp_topk_regs(const float* v, int n, int base, int topk, float* out_v,
+                                               int* out_i) {
+  const int lane = threadIdx.x & 31;
+  float x[RV];
+#pragma unroll
+  for (int j = 0; j < RV; ++j) x[j] = lane + 32 * j < n ? v[lane + 32 * j] : -INFINITY;
+  float pv = INFINITY;
+  int pi = -1;
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      const int id = base + lane + 32 * j;
+      if (lane + 32 * j < n && ranks_ahead(pv, pi, x[j], id) && ranks_ahead(x[j], id, bv, bi)) {
+        bv = x[j];
+        bi = id;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ranks_ahead(v2, i2, bv, bi)) { bv = v2; bi = i2; }
+    }
+    if (lane == 0) { out_v[r] = bv; out_i[r] = bi; }
+    pv = bv;
+    pi = bi;
+  }
+}
+
+// warp_merge_sorted with each lane owning lists lane + 32 j (j < LPL, so
+// nlists <= 32 LPL): their head positions and head pairs live in registers;
+// a round compares them, takes the shuffle argmax (with the owning lane), and
+// only the winning lane reads its list's next pair.
+template <int LPL>
+__device__ __forceinline__ void warp_merge_sorted_regs(const float* v, const int* idx, int nlists, int len, int topk,
+                                                       float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  int hpos[LPL];
+  float hv[LPL];
+  int hi[LPL];
+#pragma unroll
+  for (int j = 0; j < LPL; ++j) {
+    const int L = lane + 32 * j;
+    hpos[j] = 0;
+    const bool ok = L < nlists && len > 0;
+    hv[j] = ok ? v[L * len] : -INFINITY;
+    hi[j] = ok ? idx[L * len] : INT_MAX;
+  }
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX, bl = -1;
+#pragma unroll
+    for (int j = 0; j < LPL; ++j)
+      if (lane + 32 * j < nlists && hpos[j] < len && ranks_ahead(hv[j], hi[j], bv, bi)) {
+        bv = hv[j];
+        bi = hi[j];
+        bl = lane + 32 * j;
+      }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int l2 = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (ranks_ahead(v2, i2, bv, bi)) { bv = v2; bi = i2; bl = l2; }
+    }
+    if (lane == 0) { out_v[r] = bv; out_i[r] = bi; }
+    // the owner of the winning list moves to its next pair
+    if (bl >= 0 && (bl & 31) == lane) {
+#pragma unroll
+      for (int j = 0; j < LPL; ++j)
+        if (bl == lane + 32 * j) {
+          const int p = ++hpos[j];
+          hv[j] = p < len ? v[bl * len + p] : -INFINITY;
+          hi[j] = p < len ? idx[bl * len + p] : INT_MAX;
+        }
+    }
+  }
+}
+
 // Warp-level merge of `nlists` lists, each sorted best first and `len` long
 // (v/idx[list * len + j]), into the best `topk` (lane 0 writes out_v/out_i).
 // Each round compares only the lists' current heads; hp[] (shared memory,
@@ -298,7 +384,10 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
       const int b = b0 + bb;
       if (b >= B) continue;
       const size_t row = ((size_t)b * K + k) * ctas + blockIdx.x;
-      warp_topk(zs + bb * cap, nullptr, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
+      if (n <= 32 * 12)
+        warp_topk_regs<12>(zs + bb * cap, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
+      else
+        warp_topk(zs + bb * cap, nullptr, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
     }
     if (top_v) {
       // The last CTA of this head (in this batch pass) merges every CTA's
@@ -347,7 +436,11 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
           const int b = b0 + bb;
           if (b >= B) continue;
           const size_t o = ((size_t)b * K + k) * topk;
-          warp_merge_sorted(mv + bb * ctas * topk, mi + bb * ctas * topk, ctas, topk, topk, hp + warp * ctas,
+          if (ctas <= 32 * 4)
+            warp_merge_sorted_regs<4>(mv + bb * ctas * topk, mi + bb * ctas * topk, ctas, topk, topk, top_v + o,
+                                      top_i + o);
+          else
+            warp_merge_sorted(mv + bb * ctas * topk, mi + bb * ctas * topk, ctas, topk, topk, hp + warp * ctas,
                             top_v + o, top_i + o);
         }
         if (threadIdx.x == 0) *cnt = 0;
