@@ -129,17 +129,84 @@ __device__ __forceinline__ void warp_topk(const float* v, const int* idx, int n,
   }
 }
 
+// Bitonic sort of one (value, index) pair per lane across the warp, best
+// first (value descending, index ascending): afterwards lane r holds the
+// pair of rank r.  Every lane must take part.
+__device__ __forceinline__ void warp_sort32(float& v, int& id) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+      const int oi = __shfl_xor_sync(0xffffffffu, id, j);
+      // in a block of k lanes sorted best-first (bit k clear) the lower lane
+      // of each pair keeps the better element; in the others, the worse
+      const bool keep_better = ((lane & j) == 0) == ((lane & k) == 0);
+      if (keep_better == ranks_ahead(ov, oi, v, id)) { v = ov; id = oi; }
+    }
+  }
+}
+
 // warp_topk with the values held in registers: lane l keeps v[l + 32 j],
-// j < RV (n <= 32 RV), read from shared memory once, so a round is register
-// compares and the shuffle argmax, not a pass of dependent shared-memory
-// reads.  Same ranking and output as warp_topk (idx null: index base + i).
+// j < RV (n <= 32 RV), read from shared memory once.  Same ranking and output
+// as warp_topk (idx null: index base + i).  First a threshold: the lanes'
+// best pairs are distinct elements, so the topk-th best of them, (T, Ti),
+// ranks at or behind the row's topk-th best, and every top-k pair ranks at or
+// ahead of it; when at most 32 pairs do (the usual case), they go through
+// s_v / s_i (32 entries of shared memory) into one warp sort.  Otherwise topk
+// rounds of register compares and the shuffle argmax.  Both keep the
+// dependent shuffle steps few: at the end of a streaming pass, with other
+// CTAs still loading, each one waits behind their memory traffic.
 template <int RV>
-__device__ __forceinline__ void warp_topk_regs(const float* v, int n, int base, int topk, float* out_v,
-                                               int* out_i) {
+__device__ __forceinline__ void warp_topk_regs(const float* v, int n, int base, int topk, float* out_v, int* out_i,
+                                               float* s_v, int* s_i) {
   const int lane = threadIdx.x & 31;
   float x[RV];
 #pragma unroll
   for (int j = 0; j < RV; ++j) x[j] = lane + 32 * j < n ? v[lane + 32 * j] : -INFINITY;
+  float lv = -INFINITY;
+  int li = INT_MAX;
+#pragma unroll
+  for (int j = 0; j < RV; ++j)
+    if (lane + 32 * j < n && ranks_ahead(x[j], base + lane + 32 * j, lv, li)) {
+      lv = x[j];
+      li = base + lane + 32 * j;
+    }
+  warp_sort32(lv, li);
+  const float T = __shfl_sync(0xffffffffu, lv, topk - 1);
+  const int Ti = __shfl_sync(0xffffffffu, li, topk - 1);
+  auto cand = [&](int j) {
+    const int id = base + lane + 32 * j;
+    return lane + 32 * j < n && (ranks_ahead(x[j], id, T, Ti) || (x[j] == T && id == Ti));
+  };
+  int c = 0;
+#pragma unroll
+  for (int j = 0; j < RV; ++j) c += cand(j) ? 1 : 0;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total <= 32) {
+    int pos = incl - c;
+#pragma unroll
+    for (int j = 0; j < RV; ++j)
+      if (cand(j)) {
+        s_v[pos] = x[j];
+        s_i[pos] = base + lane + 32 * j;
+        ++pos;
+      }
+    __syncwarp();
+    float cv = lane < total ? s_v[lane] : -INFINITY;
+    int ci = lane < total ? s_i[lane] : INT_MAX;
+    __syncwarp();
+    warp_sort32(cv, ci);
+    if (lane < topk) { out_v[lane] = cv; out_i[lane] = ci; }
+    return;
+  }
   float pv = INFINITY;
   int pi = -1;
   for (int r = 0; r < topk; ++r) {
@@ -272,6 +339,8 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
                   int n_counters, float* __restrict__ top_v, int* __restrict__ top_i) {
   extern __shared__ float xs[];  // [BB][C], then [BB][cap]
   __shared__ int s_last;
+  __shared__ float s_tv[kFirst ? 1 : kGemvWarps][32];  // a ranking warp's threshold candidates
+  __shared__ int s_ti[kFirst ? 1 : kGemvWarps][32];
   // Balanced contiguous row ranges: CTA, then warp (launch parameters only).
   const int ctas = gridDim.x;
   const int cap = (rows_per_head + ctas - 1) / ctas;
@@ -385,7 +454,8 @@ heads_gemv_kernel(const TW* __restrict__ W, const TW* __restrict__ h, const floa
       if (b >= B) continue;
       const size_t row = ((size_t)b * K + k) * ctas + blockIdx.x;
       if (n <= 32 * 12)
-        warp_topk_regs<12>(zs + bb * cap, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
+        warp_topk_regs<12>(zs + bb * cap, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk, s_tv[warp],
+                           s_ti[warp]);
       else
         warp_topk(zs + bb * cap, nullptr, n, r_lo, topk, cand_v + row * topk, cand_i + row * topk);
     }
@@ -533,24 +603,6 @@ __device__ __forceinline__ void block_best(float& v, int& id, float* sv, int* si
   __syncthreads();
 }
 
-// Bitonic sort of one (value, index) pair per lane across the warp, best
-// first (value descending, index ascending): afterwards lane r holds the
-// pair of rank r.  Every lane must take part.
-__device__ __forceinline__ void warp_sort32(float& v, int& id) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
-      const int oi = __shfl_xor_sync(0xffffffffu, id, j);
-      // in a block of k lanes sorted best-first (bit k clear) the lower lane
-      // of each pair keeps the better element; in the others, the worse
-      const bool keep_better = ((lane & j) == 0) == ((lane & k) == 0);
-      if (keep_better == ranks_ahead(ov, oi, v, id)) { v = ov; id = oi; }
-    }
-  }
-}
 
 __global__ void __launch_bounds__(kRowThreads)
 topk_rows_kernel(const float* __restrict__ x, int n, int topk, float* __restrict__ out_v, int* __restrict__ out_i) {
